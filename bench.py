@@ -1,0 +1,399 @@
+"""Benchmark of the block-scaled fp8 GEMM path on one GB300.
+
+Headline workload: the weight-only fp8 decode GEMM, M=16, N=K=4096 (bf16
+activations ~N(0,1) used unquantised, e4m3 weights from N(0,0.02) with one fp32
+scale per 128x128 block, fp32 accumulate, bf16 out, seed 1).  One step = one
+call of r9q_gemm_fp8w_bf16a.  value = achieved HBM GB/s (algorithmic bytes per
+call / time per call); ms_per_step gives the us/call.
+
+Timing: every step reads its own copy of weights and activations, rotating
+over enough copies (> 3x the 129 MB L2) that each call streams from HBM; K
+calls are captured in CUDA graphs and replayed; CUDA events on the replay
+stream bracket exactly K steps, with a device synchronise on both sides.  SM
+clocks and throttle reasons are sampled through NVML (read-only) during the
+timed region.  A sweep over the other configurations follows the headline.
+
+--impl reference times the CPU oracle (test infrastructure, single thread) on a
+bounded sample of the same workload and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", FALLBACK_HBM), d.get("bf16_tflops", FALLBACK_BF16), "measured"
+    return FALLBACK_HBM, FALLBACK_BF16, "fallback"
+
+
+def gemm_bytes(M, N, K):
+    """Algorithmic bytes per call: e4m3 W + fp32 block scales + bf16 A in + bf16 Y out."""
+    return N * K + 4 * (N // 128) * (K // 128) + 2 * M * K + 2 * M * N
+
+
+def mlp_bytes(M, H, I, Ho):
+    return gemm_bytes(M, 2 * I, H) - 2 * M * 2 * I + 2 * M * I + gemm_bytes(M, Ho, I) - 2 * M * I + 2 * M * I
+
+
+# ------------------------------------------------------------- NVML clocks --
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons with NVML through ctypes (reads only)."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index=0, period_s=0.002):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.period = period_s
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mx))   # NVML_CLOCK_SM
+            self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _one(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, ctypes.c_int(1), ctypes.byref(c))
+        self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r))
+        return c.value, r.value
+
+    def start(self):
+        self.samples, self.reasons, self._stop = [], 0, False
+        if not self.ok:
+            return
+
+        def run():
+            while not self._stop:
+                c, r = self._one()
+                self.samples.append(c)
+                self.reasons |= r
+                time.sleep(self.period)
+        self._t = threading.Thread(target=run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        self._stop = True
+        self._t.join()
+        if not self.samples:
+            self.samples.append(self._one()[0])
+        names = [n for b, n in self.REASONS.items() if self.reasons & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def _make_inputs(torch, r9q, kind, M, N, K, seed, p, factor, copies, dev):
+    import synth
+    xb = synth.to_bf16_bits(synth.activations(seed, M, K, p, factor))
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    wq, ws = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(seed, N, K)).to(dev))
+    W = [wq] + [wq.clone() for _ in range(copies - 1)]
+    S = [ws] + [ws.clone() for _ in range(copies - 1)]
+    X = [x] + [x.clone() for _ in range(copies - 1)]
+    Y = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    return X, W, S, Y
+
+
+def _copies_for(bytes_per_call):
+    return max(2, math.ceil(3 * L2_BYTES / bytes_per_call))
+
+
+def _graph(torch, fn, n_calls, copies, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            fn(i % copies)
+    return g
+
+
+def _time_steps(torch, fn, K, copies, stream, sampler=None):
+    """Replay graphs covering exactly K calls; returns (ms_total)."""
+    G = copies * max(1, 64 // copies)
+    reps, rem = divmod(K, G)
+    g_full = _graph(torch, fn, G, copies, stream) if reps else None
+    g_rem = _graph(torch, fn, rem, copies, stream) if rem else None
+    if g_full:
+        g_full.replay()        # upload
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return e0.elapsed_time(e1), clocks
+
+
+def run_gpu(args):
+    import torch
+    import block_scaled_fp8_x128_gb300 as r9q
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm, bf16, src = peaks()
+    fp8_peak = 2.0 * bf16           # nominal fp8:bf16 dense ratio of 2 on the measured bf16 peak
+    stream = torch.cuda.Stream()
+
+    # ---- headline: weight-only decode GEMM, M=16, N=K=4096, seed 1 ----
+    M, N, K_ = 16, 4096, 4096
+    bpc = gemm_bytes(M, N, K_)
+    copies = _copies_for(bpc)
+    X, W, S, Y = _make_inputs(torch, r9q, "w8bf16", M, N, K_, 1, 0.0, 1.0, copies, dev)
+
+    def step(i):
+        r9q.r9q_gemm_fp8w_bf16a(X[i], W[i], S[i], y=Y[i])
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i % copies)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    ms, clocks = _time_steps(torch, step, args.steps, copies, stream, sampler)
+    us_call = ms * 1e3 / args.steps
+    gbs = bpc / (us_call * 1e-6) / 1e9
+
+    # ---- e2e: host (pinned) activations in, bf16 result out, through the same call ----
+    hx = [X[0].cpu().pin_memory() for _ in range(copies)]
+    hy = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(copies)]
+
+    def e2e_step(i):
+        X[i].copy_(hx[i], non_blocking=True)
+        r9q.r9q_gemm_fp8w_bf16a(X[i], W[i], S[i], y=Y[i])
+        hy[i].copy_(Y[i], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i % copies)
+    torch.cuda.synchronize()
+    ms_e2e, _ = _time_steps(torch, e2e_step, args.steps, copies, stream)
+    us_e2e = ms_e2e * 1e3 / args.steps
+    h2d = M * K_ * 2
+    d2h = M * N * 2
+
+    out = {
+        "metric": "block-fp8 GEMM us/call & achieved HBM GB/s (M=1..16), fp8 TFLOPS (M=8192)",
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": us_call / 1e3,
+        "us_per_call": round(us_call, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 weights x bf16 activations, fp32 accumulate",
+        "data": "synthetic (seeded splitmix64/Box-Muller: x~N(0,1) bf16, W~N(0,0.02) fp32 -> e4m3 + 128x128 fp32 scales)",
+        "config": {"workload": "weight-only fp8 decode GEMM M=16 N=4096 K=4096 (seed 1)",
+                   "M": M, "N": N, "K": K_, "bytes_per_call": bpc,
+                   "l2": f"rotating {copies} weight/activation copies ({copies * bpc / 1e6:.0f} MB > 129 MB L2)",
+                   "timing": "CUDA-graph replay of exactly K calls, CUDA events on the replay stream"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback"},
+        "e2e": {"value": round(bpc / (us_e2e * 1e-6) / 1e9, 1), "unit": "GB/s", "us_per_call": round(us_e2e, 3),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per step: pinned-host activations -> device, r9q_gemm_fp8w_bf16a, bf16 result -> pinned host; weights resident"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    del X, W, S, Y
+    torch.cuda.empty_cache()
+
+    if not args.no_sweep:
+        out["sweep"] = sweep(torch, r9q, stream, hbm, fp8_peak, src)
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    return out
+
+
+def sweep(torch, r9q, stream, hbm, fp8_peak, src):
+    res = []
+    dev = torch.device("cuda", 0)
+
+    def timeit(fn, copies, calls):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i % copies)
+        torch.cuda.synchronize()
+        ms, _ = _time_steps(torch, fn, calls, copies, stream)
+        return ms * 1e3 / calls
+
+    cases = [("c0", "w8a8", 1, 512, 1024, 0.01, 20.0, 0)]
+    cases += [("c2", "w8a8", m, 12288, 4096, 0.005, 50.0, 2) for m in (1, 2, 4, 8, 16)]
+    cases += [("c4", "w8a8", m, 4096, 4096, 0.0, 1.0, 4) for m in (32, 64, 128, 255, 8192)]
+    for name, kind, M, N, K, p, fac, seed in cases:
+        bpc = gemm_bytes(M, N, K)
+        copies = min(_copies_for(bpc), 64)
+        X, W, S, Y = _make_inputs(torch, r9q, kind, M, N, K, seed, p, fac, copies, dev)
+
+        def fn(i):
+            r9q.r9q_gemm_fp8_block_qa(X[i], W[i], S[i], y=Y[i])
+        calls = 2000 if M <= 255 else 20
+        us = timeit(fn, copies, calls)
+        flops = 2.0 * M * N * K
+        res.append({"config": name, "mode": "W8A8 fused quant", "M": M, "N": N, "K": K, "us_per_call": round(us, 3),
+                    "GBps": round(bpc / us / 1e3, 1), "frac_hbm": round(bpc / us / 1e3 / hbm, 4),
+                    "TFLOPS": round(flops / us / 1e6, 2), "frac_fp8_nominal": round(flops / us / 1e6 / fp8_peak, 4)})
+        del X, W, S, Y
+        torch.cuda.empty_cache()
+
+    # c3: fused expert MLP M=8, H=4096, I=1536, H_out=4096
+    import synth
+    M, H, I, Ho = 8, 4096, 1536, 4096
+    bpc = mlp_bytes(M, H, I, Ho)
+    copies = _copies_for(bpc)
+    xb = synth.to_bf16_bits(synth.activations(3, M, H))
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    wgu, sgu = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(3, 2 * I, H, tensor=1)).to(dev))
+    wdn, sdn = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(3, Ho, I, tensor=2)).to(dev))
+    WG = [wgu.clone() for _ in range(copies)]
+    WD = [wdn.clone() for _ in range(copies)]
+    HB = [torch.empty((M, I), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    YB = [torch.empty((M, Ho), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    for flags, label in ((0, "fused"), (r9q.R9Q_MLP_UNFUSED, "separate launches")):
+        ws_b = r9q.r9q_workspace_bytes(r9q.R9Q_OP_GATE_UP_SWIGLU_DOWN, M, I, H, Ho, flags)
+        wsp = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
+
+        def fn(i, flags=flags, wsp=wsp):
+            r9q.r9q_gate_up_swiglu_down(x, WG[i], sgu, WD[i], sdn, y=YB[i], h=HB[i], flags=flags, workspace=wsp)
+        us = timeit(fn, copies, 2000)
+        res.append({"config": "c3", "mode": f"expert MLP W8A8 ({label})", "M": M, "H": H, "I": I, "H_out": Ho,
+                    "us_per_call": round(us, 3), "GBps": round(bpc / us / 1e3, 1),
+                    "frac_hbm": round(bpc / us / 1e3 / hbm, 4)})
+    return res
+
+
+# ---------------------------------------------------------- CPU baseline --
+
+def cpu_baseline(budget_s=10.0, steps=None):
+    """The oracle as it stands (single-threaded C, -O2) on the headline workload:
+    whole M=16 x N=4096 x K=4096 weight-only calls, repeated until the budget."""
+    import oracle
+    import synth
+    M, N, K = 16, 4096, 4096
+    xb = synth.to_bf16_bits(synth.activations(1, M, K))
+    wq, ws = oracle.quant_block128(synth.weights(1, N, K))
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.gemm_w8bf16(xb, wq, ws)
+        calls += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and calls >= steps) or (steps is None and el >= budget_s):
+            break
+    us = el * 1e6 / calls
+    return {"value": round(gemm_bytes(M, N, K) / us / 1e3, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "us_per_call": round(us, 1),
+            "sample": f"{calls} whole M=16 N=4096 K=4096 weight-only calls of the C oracle, 1 thread"}
+
+
+def run_reference(args):
+    """The oracle on the host cores, on bounded per-step samples of the headline
+    workload: each step = one token row x all 4096 outputs x K=4096."""
+    import oracle
+    import synth
+    M, N, K = 16, 4096, 4096
+    xb = synth.to_bf16_bits(synth.activations(1, M, K))
+    wq, ws = oracle.quant_block128(synth.weights(1, N, K))
+    rows_per_step = 1
+    for i in range(args.warmup):
+        oracle.gemm_w8bf16(xb, wq, ws, rows=np.array([i % M]))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm_w8bf16(xb, wq, ws, rows=np.array([i % M]))
+    el = time.perf_counter() - t0
+    # a full call is M rows; scale the per-row time to a call
+    us_call = el * 1e6 / args.steps * (M / rows_per_step)
+    gbs = gemm_bytes(M, N, K) / us_call / 1e3
+    return {"impl": "reference", "metric": "block-fp8 GEMM us/call & achieved HBM GB/s (M=1..16), fp8 TFLOPS (M=8192)",
+            "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": "weight-only fp8 decode GEMM M=16 N=4096 K=4096 (seed 1)"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} steps of one token row x 4096 outputs x K=4096"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="r9q", choices=["r9q", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        # replicas only: the path does not shard across GPUs here; every rank
+        # runs the same single-GPU step and rank 0 reports the aggregate
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    out = run_gpu(args)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([out["ms_per_step"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        out["ms_per_step"] = t.item()
+        out["n_gpus"] = world
+        out["value"] = round(out["value"] * world, 1)
+    if rank == 0:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

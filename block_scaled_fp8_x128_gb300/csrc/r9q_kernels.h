@@ -1,0 +1,66 @@
+// Internal launch interface between the C ABI (r9q_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace r9q {
+
+// ---- stream (decode-width) GEMM ----
+enum AMode : int { A_QUANT = 0, A_PREQ = 1, A_BF16 = 2 };
+enum Epi : int { EPI_STORE = 0, EPI_SWIGLU = 1 };
+
+constexpr int kStages = 4;                       // weight ring depth
+constexpr int kCWarps = 4;                       // consumer (MMA) warps
+constexpr int kStreamThreads = (kCWarps + 1) * 32;
+constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m3)
+constexpr int kPStride = 128 + 4;                // fp32 partial row stride (floats)
+
+struct StreamParams {
+    const uint16_t* a;   // bf16 activations [M][K]          (A_QUANT, A_BF16)
+    uint8_t* aq;         // e4m3 [M][K]: input (A_PREQ) / optional output (A_QUANT)
+    float* as;           // fp32 [M][KB]: input (A_PREQ) / optional output (A_QUANT)
+    const float* ws;     // fp32 [NB][KB] weight block scales
+    uint16_t* y;         // bf16 output [M][ldy] (EPI_STORE: y, EPI_SWIGLU: h)
+    int M, K, KB, ldy;
+    int splits;          // K splits = cluster size
+    int* err;            // device error word
+};
+
+struct StreamPlan {
+    int MT;              // token tile: 8, 16, 32 or 64
+    int splits;          // cluster size along K
+    int ntiles;          // 128-row weight tiles
+    int mchunks;         // ceil(M / MT)
+    size_t smem;         // dynamic shared memory bytes
+};
+
+size_t stream_smem_bytes(int MT, int amode, int kbs_max);
+// Chooses MT and the split count; returns false when no configuration fits.
+bool plan_stream(int64_t M, int64_t N, int64_t K, int amode, int sms, StreamPlan* plan);
+
+cudaError_t launch_stream(const StreamPlan& plan, int amode, int epi, const CUtensorMap& wmap,
+                          const StreamParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_stream_a_quant(const StreamPlan& plan, int epi, const CUtensorMap& wmap,
+                                  const StreamParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_stream_a_preq(const StreamPlan& plan, int epi, const CUtensorMap& wmap,
+                                 const StreamParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_stream_a_bf16(const StreamPlan& plan, int epi, const CUtensorMap& wmap,
+                                 const StreamParams& p, cudaStream_t st, bool pdl);
+
+// Raises a kernel's dynamic shared memory limit once per device (the attribute
+// is not touched again afterwards, so launches can be captured in graphs).
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+// ---- elementwise / quantisation ----
+cudaError_t launch_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, cudaStream_t st, int sms);
+cudaError_t launch_quant_group128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
+                                  cudaStream_t st, int sms);
+cudaError_t launch_quant_weight_block128(const float* w, int64_t N, int64_t K, uint8_t* wq, float* ws,
+                                         cudaStream_t st);
+cudaError_t launch_swiglu_interleaved(const uint16_t* gu, int64_t M, int64_t I, uint16_t* h,
+                                      cudaStream_t st, int sms);
+
+}  // namespace r9q

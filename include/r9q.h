@@ -1,0 +1,155 @@
+/*
+ * r9q.h — C ABI of libr9q.so: block-scaled fp8 (e4m3) GEMMs for GB300 (sm_103a).
+ *
+ * The operation: a GEMM y[M][N] = x[M][K] * w[N][K]^T whose weights are OCP
+ * FP8 E4M3 codes with one fp32 scale per 128x128 block, accumulated in fp32
+ * and written as bf16.  Two modes:
+ *   W8A8        — each token's activations are quantised per 128-wide K group
+ *                 (scale = amax/448 in fp32, q = e4m3(x/scale) rounded to
+ *                 nearest even, saturating to +-448) inside the GEMM's A-load,
+ *                 byte-identical to a separate quantisation pass
+ *                 (r9700-stack v0.3.1 release notes, "What changed for someone
+ *                 running it": fused activation quant in the dense fp8 block
+ *                 GEMM, "=0 splits it again");
+ *   weight-only — the fp8 weights against the unquantised bf16 activations
+ *                 (same notes: fp8 hyper-connection decode GEMMs, bf16 MMA
+ *                 against the unquantised activations).
+ * Plus a fused expert MLP: silu(gate)*up in the gate_up GEMM's epilogue and the
+ * fp8 row quantisation of that result in the down GEMM's A-load (releases page,
+ * v0.3.3 "What changed": the fused MoE decode path).
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates device memory and keeps no pointer after a call returns.
+ *  - Matrices are row-major and contiguous.  bf16 is passed as void* (16-bit
+ *    IEEE bfloat16).  e4m3 codes are uint8_t.
+ *  - Data pointers (bf16 / e4m3 / outputs) must be 16-byte aligned; fp32
+ *    scale pointers 4-byte aligned.
+ *  - N, K (and H, I, H_out) must be positive multiples of 128; M >= 1.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous: a return of 0 means "enqueued".
+ *  - Outputs never alias inputs.  Outputs are fully overwritten.
+ *  - Errors are negative return codes (below); on an error nothing has been
+ *    enqueued and no CUDA state is changed.  A device-side wait that times out
+ *    (it never should) sets a device error word readable with
+ *    r9q_last_device_error.
+ *  - Calls on one stream are ordered; a workspace may not be shared by calls
+ *    that can run concurrently on different streams.
+ */
+#ifndef R9Q_H_
+#define R9Q_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define R9Q_VERSION 1
+
+/* return codes */
+#define R9Q_OK              0
+#define R9Q_ERR_NULL       -1   /* a required pointer is NULL */
+#define R9Q_ERR_DIM        -2   /* bad or unsupported dimensions */
+#define R9Q_ERR_ALIGN      -3   /* pointer misaligned */
+#define R9Q_ERR_WORKSPACE  -4   /* workspace missing or too small */
+#define R9Q_ERR_LAUNCH     -5   /* CUDA launch / runtime error */
+#define R9Q_ERR_TIMEOUT    -6   /* a bounded device wait gave up */
+#define R9Q_ERR_DEVICE     -7   /* current device is not sm_103 */
+#define R9Q_ERR_ARG        -8   /* other invalid argument (flags, op) */
+
+/* Library version (R9Q_VERSION). */
+int r9q_version(void);
+
+/* Human-readable text for a return code; never NULL. */
+const char* r9q_strerror(int code);
+
+/* Reads and clears the device error word after synchronising `stream`.
+ * Returns 0 when no kernel has reported an error since the last call,
+ * otherwise the recorded negative code (R9Q_ERR_TIMEOUT). */
+int r9q_last_device_error(void* stream);
+
+/* fp32 -> e4m3 conversion used by every quantiser: round to nearest even,
+ * saturating to +-448 (OCP FP8 E4M3; the saturation rule of the operation's
+ * statement).  x: n floats, q: n bytes.  n >= 0 (0 is a no-op). */
+int r9q_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, void* stream);
+
+/* Per-token-group-128 activation quantisation (the separate pass of the
+ * unfused W8A8 path; r9700-stack v0.3.1 notes, fused activation quant "=0
+ * splits it again").  x_bf16[M][K] -> xq[M][K] e4m3 codes and
+ * xs[M][K/128] fp32 scales, s = amax/448 (fp32 division), q = e4m3(x/s) with
+ * one fp32 division per element; an all-zero group gives s = 0 and codes 0. */
+int r9q_quant_group128(const void* x_bf16, int64_t M, int64_t K,
+                       uint8_t* xq, float* xs, void* stream);
+
+/* Weight quantisation with one fp32 scale per 128x128 block (set-up, not the
+ * hot path): w[N][K] fp32 -> wq[N][K] e4m3, ws[N/128][K/128] fp32,
+ * s = amax/448 over the block, q = e4m3(w/s). */
+int r9q_quant_weight_block128(const float* w, int64_t N, int64_t K,
+                              uint8_t* wq, float* ws, void* stream);
+
+/* W8A8 block-fp8 GEMM (r9700-stack v0.3.1 notes: r9k_gemm_fp8_block_qa;
+ * v0.3.0 notes: exact block-scaled fp8 GEMM).
+ *   y[m][n] = bf16( sum_kb P[m][n][kb] * as[m][kb] * ws[n/128][kb] ),
+ *   P[m][n][kb] = sum_{k in block kb} e4m3(aq[m][k]) * e4m3(w[n][k]) in fp32.
+ * Fused mode (a_bf16 != NULL): the activations are quantised per token and
+ *   128-wide K group inside the kernel; aq[M][K] / as[M][K/128] are then
+ *   OPTIONAL outputs (either both NULL or both set) that receive exactly the
+ *   bytes and scales r9q_quant_group128 produces.
+ * Unfused mode (a_bf16 == NULL): aq / as are required inputs.
+ * w[N][K] e4m3, ws[N/128][K/128] fp32, y_bf16[M][N].
+ * workspace: query r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, ...); when it
+ *   reports 0 bytes, workspace may be NULL. */
+int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as,
+                          const uint8_t* w, const float* ws, void* y_bf16,
+                          int64_t M, int64_t N, int64_t K,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Weight-only fp8 GEMM: y[m][n] = bf16( sum_kb (sum_{k in kb} x[m][k] * e4m3(w[n][k])) * ws[n/128][kb] )
+ * with x the unquantised bf16 activations (r9700-stack v0.3.1 notes: fp8
+ * hyper-connection decode GEMMs).  Products are exact in fp32 (the e4m3
+ * weights are converted exactly to bf16 in registers). */
+int r9q_gemm_fp8w_bf16a(const void* a_bf16, const uint8_t* w, const float* ws, void* y_bf16,
+                        int64_t M, int64_t N, int64_t K,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Flags of r9q_gate_up_swiglu_down. */
+#define R9Q_MLP_WEIGHT_ONLY 1   /* both GEMMs weight-only (no quant of x or h) */
+#define R9Q_MLP_UNFUSED     2   /* run the separate-launch chain instead of the fused one */
+
+/* Expert MLP at decode (releases page, v0.3.3 "What changed": fused MoE decode
+ * path, silu(gate)*up in the gate_up GEMM's epilogue, the fp8 row quant inside
+ * the down GEMM's A-load, outputs bit-identical to the separate-launch path).
+ *   gu = GEMM(x, w_gu) with w_gu[2I][H] holding gate and up interleaved per
+ *        128 rows: rows [256j, 256j+128) are gate block j, rows
+ *        [256j+128, 256j+256) up block j; s_gu[2I/128][H/128];
+ *   h[m][128j+c] = bf16( silu(g) * u ), g = bf16(gu[m][256j+c]),
+ *        u = bf16(gu[m][256j+128+c]);
+ *   y = GEMM(h, w_dn) with w_dn[H_out][I], s_dn[H_out/128][I/128],
+ *        h quantised per token and 128-wide group in the A-load (W8A8).
+ * Both GEMMs are W8A8 (x quantised in the gate_up A-load) unless
+ * R9Q_MLP_WEIGHT_ONLY.  h_bf16_out[M][I], hq_out[M][I], hs_out[M][I/128] are
+ * optional outputs (hq/hs only in W8A8 mode; both or neither).  R9Q_MLP_UNFUSED
+ * runs gate_up GEMM -> SwiGLU -> quant -> down GEMM as separate launches and
+ * gives bit-identical outputs.  workspace: r9q_workspace_bytes(
+ * R9Q_OP_GATE_UP_SWIGLU_DOWN, M, I, H, H_out, flags, &bytes). */
+int r9q_gate_up_swiglu_down(const void* x_bf16,
+                            const uint8_t* w_gu, const float* s_gu,
+                            const uint8_t* w_dn, const float* s_dn,
+                            void* y_bf16, int64_t M, int64_t H, int64_t I, int64_t H_out,
+                            void* h_bf16_out, uint8_t* hq_out, float* hs_out, int flags,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace query. */
+#define R9Q_OP_GEMM_W8A8            1   /* (M, N, K) */
+#define R9Q_OP_GEMM_W8BF16          2   /* (M, N, K) */
+#define R9Q_OP_GATE_UP_SWIGLU_DOWN  3   /* (M, N=I, K=H, N2=H_out, flags) */
+/* Writes the bytes of device workspace the call needs (0 = none) to *bytes. */
+int r9q_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t N2, int flags,
+                        size_t* bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* R9Q_H_ */

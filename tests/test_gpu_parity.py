@@ -1,0 +1,279 @@
+"""GPU parity: every entry point of libr9q, called through the C ABI binding,
+against the CPU oracle on the same seeded inputs.
+
+  * e4m3 conversion, group-128 quant and weight block quant: bit-exact;
+  * GEMM outputs: |gpu - ref| <= 8e-3 |ref| + 1e-3 max|ref| per element, ref =
+    the oracle's fp32 accumulator on the same (bit-identical) quantised operands;
+  * fused vs unfused quant: identical bytes, scales and outputs;
+  * fused expert MLP vs the separate-launch chain: identical h, hq, hs, y.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _helpers import (activations_bf16, assert_close, bf16_to_dev, bits_of, dev, f32_of_bits,
+                      quantised_weights)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def r9q():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_scaled_fp8_x128_gb300 as lib
+    return lib
+
+
+# ------------------------------------------------------------------ codec --
+
+def test_codec_dense_range(r9q):
+    """Every fp32 pattern with |x| in [2^-12, 2^10), both signs, plus samples of
+    all other finite patterns: GPU cvt.rn.satfinite == oracle codec."""
+    lo = int(np.float32(2.0 ** -12).view(np.uint32))
+    hi = int(np.float32(2.0 ** 10).view(np.uint32))
+    step = 1 << 24
+    for sign in (0, 0x80000000):
+        for start in range(lo, hi, step):
+            n = min(step, hi - start)
+            ref = oracle.e4m3_encode_bits(start | sign, n)
+            pat = np.arange(start, start + n, dtype=np.uint32) | np.uint32(sign)
+            q = r9q.r9q_e4m3_from_f32(torch.from_numpy(pat.view(np.float32)).to(dev()))
+            got = q.cpu().numpy()
+            bad = np.nonzero(got != ref)[0]
+            assert bad.size == 0, [(hex((start | sign) + int(i)), got[i], ref[i]) for i in bad[:5]]
+
+
+def test_codec_sampled_all_patterns(r9q):
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 1 << 32, size=4_000_000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    x = np.concatenate([x, np.float32([0.0, -0.0, 448, 464, -464, 480, 1e38, -1e38, 1e-45])])
+    got = r9q.r9q_e4m3_from_f32(torch.from_numpy(x).to(dev())).cpu().numpy()
+    assert np.array_equal(got, oracle.e4m3_encode_array(x))
+    # tail handling (n not a multiple of 4)
+    got7 = r9q.r9q_e4m3_from_f32(torch.from_numpy(x[:7].copy()).to(dev())).cpu().numpy()
+    assert np.array_equal(got7, oracle.e4m3_encode_array(x[:7]))
+
+
+# ---------------------------------------------------------- group quant --
+
+@pytest.mark.parametrize("M,K,p,factor,seed", [
+    (1, 1024, 0.01, 20.0, 0),        # c0 activations
+    (16, 4096, 0.005, 50.0, 2),      # c2 activations
+    (3, 384, 0.0, 1.0, 7),           # ragged M, few groups
+    (255, 4096, 0.0, 1.0, 4),        # c4 M=255
+])
+def test_quant_group128_bit_exact(r9q, M, K, p, factor, seed):
+    xb = activations_bf16(seed, M, K, p, factor)
+    if M >= 3:
+        xb[0, 128:256] = 0                                         # zero group
+        xb[1, 0:128] = synth.to_bf16_bits(np.full(128, 1e-38, np.float32))  # subnormal scale
+        xb[2, 0] = synth.to_bf16_bits(np.float32([448.0]))[0]      # amax exactly 448 ...
+        xb[2, 1:128] = synth.to_bf16_bits(np.float32(np.linspace(-3, 3, 127)))
+        xb[2, 5] = 0x8000                                          # ... with a -0.0 inside
+    xq, xs = r9q.r9q_quant_group128(bf16_to_dev(xb))
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_group(xb)
+    assert np.array_equal(xs.cpu().numpy(), os_)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+
+
+def test_weight_block_quant_bit_exact(r9q):
+    quantised_weights(r9q, 0, 512, 1024)
+    quantised_weights(r9q, 1, 4096, 4096)
+    # a block of zeros gives scale 0 and codes 0
+    w = np.zeros((256, 256), np.float32)
+    w[128:, :128] = synth.weights(9, 128, 128)
+    wq, ws = r9q.r9q_quant_weight_block128(torch.from_numpy(w).to(dev()))
+    oq, os_ = oracle.quant_block128(w)
+    assert np.array_equal(wq.cpu().numpy(), oq) and np.array_equal(ws.cpu().numpy(), os_)
+
+
+# ---------------------------------------------------------------- W8A8 --
+
+def _w8a8_case(r9q, M, N, K, p, factor, seed, rows=None):
+    xb = activations_bf16(seed, M, K, p, factor)
+    wq, ws = quantised_weights(r9q, seed, N, K)
+    x = bf16_to_dev(xb)
+    aq = torch.empty((M, K), dtype=torch.uint8, device=dev())
+    a_s = torch.empty((M, K // 128), dtype=torch.float32, device=dev())
+    y = r9q.r9q_gemm_fp8_block_qa(x, wq, ws, aq=aq, as_=a_s)
+    # unfused: separate quant pass, then the GEMM on (aq, as)
+    uq, us = r9q.r9q_quant_group128(x)
+    yu = r9q.r9q_gemm_fp8_block_qa(None, wq, ws, aq=uq, as_=us)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_group(xb)
+    assert np.array_equal(aq.cpu().numpy(), oq), "fused A-load quant codes != oracle"
+    assert np.array_equal(a_s.cpu().numpy(), os_), "fused A-load quant scales != oracle"
+    assert torch.equal(aq, uq) and torch.equal(a_s, us), "fused and unfused quant operands differ"
+    assert torch.equal(y.view(torch.int16), yu.view(torch.int16)), "fused and unfused outputs differ"
+    acc, _ = oracle.gemm_w8a8(oq, os_, wq.cpu().numpy(), ws.cpu().numpy(), rows=rows)
+    yb = bits_of(y)
+    if rows is not None:
+        yb = yb[rows]
+    return assert_close(yb, acc, f"W8A8 M={M} N={N} K={K}")
+
+
+def test_w8a8_c0(r9q):
+    _w8a8_case(r9q, 1, 512, 1024, 0.01, 20.0, 0)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_w8a8_c2(r9q, M):
+    _w8a8_case(r9q, M, 12288, 4096, 0.005, 50.0, 2)
+
+
+@pytest.mark.parametrize("M", [32, 64, 128, 255])
+def test_w8a8_c4(r9q, M):
+    _w8a8_case(r9q, M, 4096, 4096, 0.0, 1.0, 4)
+
+
+def test_w8a8_c4_prefill_sampled(r9q):
+    rows = np.array([0, 1, 127, 128, 1000, 4095, 4096, 6001, 8190, 8191])
+    _w8a8_case(r9q, 8192, 4096, 4096, 0.0, 1.0, 4, rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 256, 384), (5, 384, 640), (13, 128, 128), (17, 640, 256),
+                                   (33, 256, 1152), (63, 384, 512), (65, 256, 512), (100, 128, 384)])
+def test_w8a8_ragged(r9q, M, N, K):
+    _w8a8_case(r9q, M, N, K, 0.01, 20.0, 11)
+
+
+# --------------------------------------------------------- weight-only --
+
+def _w8bf16_case(r9q, M, N, K, seed):
+    xb = activations_bf16(seed, M, K)
+    wq, ws = quantised_weights(r9q, seed, N, K)
+    y = r9q.r9q_gemm_fp8w_bf16a(bf16_to_dev(xb), wq, ws)
+    torch.cuda.synchronize()
+    acc, _ = oracle.gemm_w8bf16(xb, wq.cpu().numpy(), ws.cpu().numpy())
+    return assert_close(bits_of(y), acc, f"weight-only M={M} N={N} K={K}")
+
+
+def test_w8bf16_c1(r9q):
+    _w8bf16_case(r9q, 16, 4096, 4096, 1)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (3, 256, 384), (9, 384, 1280), (31, 256, 256),
+                                   (64, 128, 640), (70, 256, 256)])
+def test_w8bf16_ragged(r9q, M, N, K):
+    _w8bf16_case(r9q, M, N, K, 12)
+
+
+def test_w8bf16_every_code_exact(r9q):
+    """One-hot activations select single weight codes: y = bf16(value * ws) must
+    be exact for every finite code, subnormals included (checks the in-register
+    e4m3 -> bf16 conversion)."""
+    K, N = 256, 256
+    wq = ((np.arange(N, dtype=np.int64)[:, None] * 131 + np.arange(K)[None, :] * 7) % 256).astype(np.uint8)
+    wq[(wq & 0x7F) == 0x7F] = 0x7E
+    ws = np.array([[1.0, 2.0], [0.5, 0.25]], np.float32)
+    ks = np.arange(0, K, 1)
+    x = np.zeros((len(ks), K), np.float32)
+    x[np.arange(len(ks)), ks] = 1.0
+    xb = synth.to_bf16_bits(x)
+    y = r9q.r9q_gemm_fp8w_bf16a(bf16_to_dev(xb), torch.from_numpy(wq).to(dev()), torch.from_numpy(ws).to(dev()))
+    acc, yo = oracle.gemm_w8bf16(xb, wq, ws)
+    assert np.array_equal(bits_of(y), yo)
+    seen = set(np.unique(wq[:, ks]))
+    assert len(seen) == 254        # all finite codes exercised
+
+
+# ----------------------------------------------------------- expert MLP --
+
+@pytest.mark.parametrize("weight_only", [False, True])
+@pytest.mark.parametrize("M,H,I,Ho", [(8, 4096, 1536, 4096), (3, 256, 384, 640), (20, 512, 256, 384)])
+def test_mlp_fused_vs_unfused_and_oracle(r9q, weight_only, M, H, I, Ho):
+    seed = 3
+    xb = activations_bf16(seed, M, H)
+    wgu, sgu = quantised_weights(r9q, seed, 2 * I, H, tensor=1)
+    wdn, sdn = quantised_weights(r9q, seed, Ho, I, tensor=2)
+    x = bf16_to_dev(xb)
+    flags = r9q.R9Q_MLP_WEIGHT_ONLY if weight_only else 0
+    outs = {}
+    for unfused in (False, True):
+        h = torch.empty((M, I), dtype=torch.bfloat16, device=dev())
+        hq = None if weight_only else torch.empty((M, I), dtype=torch.uint8, device=dev())
+        hs = None if weight_only else torch.empty((M, I // 128), dtype=torch.float32, device=dev())
+        y = r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn, h=h, hq=hq, hs=hs,
+                                        flags=flags | (r9q.R9Q_MLP_UNFUSED if unfused else 0))
+        outs[unfused] = (y, h, hq, hs)
+    torch.cuda.synchronize()
+    (y0, h0, hq0, hs0), (y1, h1, hq1, hs1) = outs[False], outs[True]
+    assert torch.equal(h0.view(torch.int16), h1.view(torch.int16)), "fused h != separate-launch h"
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16)), "fused y != separate-launch y"
+    if not weight_only:
+        assert torch.equal(hq0, hq1) and torch.equal(hs0, hs1), "fused hq/hs != separate-launch hq/hs"
+    ref = oracle.gate_up_swiglu_down(xb, wgu.cpu().numpy(), sgu.cpu().numpy(), wdn.cpu().numpy(),
+                                     sdn.cpu().numpy(), weight_only=weight_only)
+    hb = bits_of(h0)
+    assert_close(hb, f32_of_bits(ref["h"]), "h")
+    assert_close(bits_of(y0), f32_of_bits(ref["y"]), "y")
+    if not weight_only:
+        # the row quant of the GPU's own h must match the oracle's quant bit for bit
+        oq, os_ = oracle.quant_group(hb)
+        assert np.array_equal(hq0.cpu().numpy(), oq) and np.array_equal(hs0.cpu().numpy(), os_)
+        # and y against the oracle's down GEMM on those operands
+        acc, _ = oracle.gemm_w8a8(oq, os_, wdn.cpu().numpy(), sdn.cpu().numpy())
+        assert_close(bits_of(y0), acc, "y from the GPU's hq")
+    else:
+        acc, _ = oracle.gemm_w8bf16(hb, wdn.cpu().numpy(), sdn.cpu().numpy())
+        assert_close(bits_of(y0), acc, "y from the GPU's h")
+
+
+def test_mlp_without_optional_outputs(r9q):
+    M, H, I, Ho = 8, 256, 256, 256
+    xb = activations_bf16(5, M, H)
+    wgu, sgu = quantised_weights(r9q, 5, 2 * I, H, tensor=1, check_oracle=False)
+    wdn, sdn = quantised_weights(r9q, 5, Ho, I, tensor=2, check_oracle=False)
+    x = bf16_to_dev(xb)
+    h = torch.empty((M, I), dtype=torch.bfloat16, device=dev())
+    y_ref = r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn, h=h)
+    y = r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn)             # h in the workspace
+    y_u = r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn, flags=r9q.R9Q_MLP_UNFUSED)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    assert torch.equal(y_u.view(torch.int16), y_ref.view(torch.int16))
+
+
+# ----------------------------------------------------------- determinism --
+
+def test_repeat_calls_bit_identical(r9q):
+    M, N, K = 16, 4096, 4096
+    xb = activations_bf16(2, M, K, 0.005, 50.0)
+    wq, ws = quantised_weights(r9q, 2, N, K, check_oracle=False)
+    x = bf16_to_dev(xb)
+    first = r9q.r9q_gemm_fp8_block_qa(x, wq, ws).clone()
+    first_w = r9q.r9q_gemm_fp8w_bf16a(x, wq, ws).clone()
+    for _ in range(50):
+        assert torch.equal(r9q.r9q_gemm_fp8_block_qa(x, wq, ws).view(torch.int16), first.view(torch.int16))
+        assert torch.equal(r9q.r9q_gemm_fp8w_bf16a(x, wq, ws).view(torch.int16), first_w.view(torch.int16))
+    assert r9q.r9q_last_device_error() == 0
+
+
+def test_graph_replay_alternating_shapes(r9q):
+    """Captured calls with different M replayed many times give the eager results."""
+    N, K = 1024, 2048
+    wq, ws = quantised_weights(r9q, 8, N, K, check_oracle=False)
+    xs = [bf16_to_dev(activations_bf16(8, M, K, tensor=M)) for M in (1, 16, 3, 8)]
+    eager = [r9q.r9q_gemm_fp8_block_qa(x, wq, ws).clone() for x in xs]
+    outs = [torch.empty_like(e) for e in eager]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for x, o in zip(xs, outs):
+            r9q.r9q_gemm_fp8_block_qa(x, wq, ws, y=o)
+    for _ in range(300):
+        g.replay()
+    torch.cuda.synchronize()
+    for e, o in zip(eager, outs):
+        assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+
+
+def test_device_error_word_clear(r9q):
+    assert r9q.r9q_last_device_error() == 0
