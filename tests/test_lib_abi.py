@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from block_scaled_fp8_x128_gb300 import build as b
-    path = b.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 
