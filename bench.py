@@ -196,22 +196,24 @@ def run_gpu(args):
     gbs = bpc / (us_call * 1e-6) / 1e9
 
     # ---- e2e: host (pinned) activations in, bf16 result out, through the same call ----
-    hx = [X[0].cpu().pin_memory() for _ in range(copies)]
-    hy = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(copies)]
-
-    def e2e_step(i):
-        X[i].copy_(hx[i], non_blocking=True)
-        r9q.r9q_gemm_fp8w_bf16a(X[i], W[i], S[i], y=Y[i])
-        hy[i].copy_(Y[i], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_step(i % copies)
-    torch.cuda.synchronize()
-    ms_e2e, _ = _time_steps(torch, e2e_step, args.steps, copies, stream)
-    us_e2e = ms_e2e * 1e3 / args.steps
     h2d = M * K_ * 2
     d2h = M * N * 2
+    us_e2e = float("nan")
+    if not args.no_e2e:
+        hx = [X[0].cpu().pin_memory() for _ in range(copies)]
+        hy = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(copies)]
+
+        def e2e_step(i):
+            X[i].copy_(hx[i], non_blocking=True)
+            r9q.r9q_gemm_fp8w_bf16a(X[i], W[i], S[i], y=Y[i])
+            hy[i].copy_(Y[i], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i % copies)
+        torch.cuda.synchronize()
+        ms_e2e, _ = _time_steps(torch, e2e_step, args.steps, copies, stream)
+        us_e2e = ms_e2e * 1e3 / args.steps
 
     out = {
         "metric": "block-fp8 GEMM us/call & achieved HBM GB/s (M=1..16), fp8 TFLOPS (M=8192)",
@@ -234,7 +236,8 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4), "traffic": None,
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback"},
-        "e2e": {"value": round(bpc / (us_e2e * 1e-6) / 1e9, 1), "unit": "GB/s", "us_per_call": round(us_e2e, 3),
+        "e2e": {"value": None if args.no_e2e else round(bpc / (us_e2e * 1e-6) / 1e9, 1), "unit": "GB/s",
+                "us_per_call": None if args.no_e2e else round(us_e2e, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step: pinned-host activations -> device, r9q_gemm_fp8w_bf16a, bf16 result -> pinned host; weights resident"},
         "gpu_launches": args.steps,
@@ -367,6 +370,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

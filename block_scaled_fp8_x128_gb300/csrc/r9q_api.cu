@@ -141,8 +141,8 @@ size_t mlp_workspace(int64_t M, int64_t I, int flags, bool have_h, bool have_hq)
 
 size_t stream_smem_bytes(int MT, int amode, int kbs_max) {
     const size_t kslice = (size_t)kbs_max * 128;
-    const size_t act_ld = (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16;
-    size_t off = (size_t)kStages * kStageBytes + 16 * kStages + 16 + 4 * (2 * (size_t)kbs_max + (size_t)MT * kbs_max);
+    const size_t act_ld = (amode == A_QUANT) ? 2 * kslice + 16 : (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16;
+    size_t off = (size_t)kStages * kStageBytes + 16 * kStages + 16 + 16 + 4 * (2 * (size_t)kbs_max + (size_t)MT * kbs_max);
     off = (off + 15) & ~static_cast<size_t>(15);
     return 1024 + off + (size_t)MT * act_ld;
 }

@@ -40,10 +40,25 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// q = e4m3(fl32(x / s)) without a division per element.  y = x * (1/s) with
+// the correctly rounded reciprocal is within 2 fp32 ulps of fl32(x/s); the
+// e4m3 rounding of a value only depends on which side of an e4m3 midpoint it
+// lies, and for |y| >= 2^-6 those midpoints are exactly the fp32 values whose
+// low 20 mantissa bits are 0x80000.  So y gives the same code unless it lies
+// within 2 ulps of such a midpoint or in the e4m3 subnormal range, and those
+// (rare) elements take the IEEE division.  `r` must be finite.
+__device__ __forceinline__ float quot_for_e4m3(float x, float s, float r) {
+    const float y = __fmul_rn(x, r);
+    const uint32_t lo = __float_as_uint(y) & 0xFFFFFu;
+    if (fabsf(y) < 0x1p-6f || (lo - 0x7FFFEu) <= 4u) return __fdiv_rn(x, s);
+    return y;
+}
+
 // Group-128 quantisation of one group held by a full warp: lane l holds
 // x[4l .. 4l+3].  scale = amax/448 (IEEE fp32 division); codes = e4m3(x/scale)
-// with one IEEE fp32 division per element; amax == 0 gives scale 0, codes 0.
-// Returns the lane's 4 codes packed little-endian (x[4l] in bits 0..7).
+// exactly as one IEEE fp32 division per element would give (see
+// quot_for_e4m3); amax == 0 gives scale 0, codes 0.  Returns the lane's 4
+// codes packed little-endian (x[4l] in bits 0..7).
 __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, float v2, float v3,
                                                         float& scale) {
     float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
@@ -52,9 +67,20 @@ __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, floa
     const float s = __fdiv_rn(amax, 448.0f);
     scale = s;
     if (amax == 0.0f) return 0u;
-    const uint32_t lo = cvt_e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
-    const uint32_t hi = cvt_e4m3x2(__fdiv_rn(v2, s), __fdiv_rn(v3, s));
-    return lo | (hi << 16);
+    const float r = __frcp_rn(s);
+    float t0, t1, t2, t3;
+    if (r < 0x1p127f) {            // finite reciprocal (s is not a tiny subnormal)
+        t0 = quot_for_e4m3(v0, s, r);
+        t1 = quot_for_e4m3(v1, s, r);
+        t2 = quot_for_e4m3(v2, s, r);
+        t3 = quot_for_e4m3(v3, s, r);
+    } else {
+        t0 = __fdiv_rn(v0, s);
+        t1 = __fdiv_rn(v1, s);
+        t2 = __fdiv_rn(v2, s);
+        t3 = __fdiv_rn(v3, s);
+    }
+    return cvt_e4m3x2(t0, t1) | (cvt_e4m3x2(t2, t3) << 16);
 }
 
 // silu(g) * u in fp32 (g, u already bf16-rounded); the separate-launch SwiGLU
@@ -134,6 +160,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 

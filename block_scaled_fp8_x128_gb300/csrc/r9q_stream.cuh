@@ -10,11 +10,13 @@
 //  * one producer thread streams 128x128 e4m3 weight tiles with 2-D TMA
 //    (128-byte swizzle) into a 4-stage shared-memory ring guarded by
 //    full/empty mbarriers; the whole ring is issued before anything else.
-//  * the CTA's activation slice sits in shared memory.  W8A8: each 128-wide
-//    group is quantised by one warp at the A-load (shuffle amax, IEEE divide,
-//    cvt.rn.satfinite.e4m3x2), byte-identical to the standalone quant kernel.
-//    Weight-only: bf16 rows, stored with each group of 4 permuted (x0,x2,x1,x3)
-//    to match the register order of the in-register e4m3 -> bf16 conversion.
+//  * the CTA's activation slice arrives in shared memory with one bulk copy
+//    per token row, issued right after the weight ring.  W8A8: each 128-wide
+//    group is then quantised in place by one warp at the A-load (shuffle amax,
+//    fp32 division-exact quotient, cvt.rn.satfinite.e4m3x2), byte-identical
+//    to the standalone quant kernel.  Weight-only: the bf16 rows are the B
+//    operand, their pairs swapped in registers to match the in-register
+//    e4m3 -> bf16 conversion.
 //  * four MMA warps run swap-AB mma.sync (weights are the 16-row A operand,
 //    tokens the 8-column B operand): m16n8k32 e4m3 for W8A8, m16n8k16 bf16
 //    for weight-only.  Each k-block's fp32 partial is promoted into register
@@ -73,12 +75,18 @@ __global__ void __launch_bounds__(kStreamThreads)
     uint8_t* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     uint64_t* empty = full + kStages;
-    int* flags = reinterpret_cast<int*>(empty + kStages);       // [0] error, [1] issued
+    uint64_t* abar = empty + kStages;                           // activation bulk copies
+    int* flags = reinterpret_cast<int*>(abar + 2);              // [0] error, [1] issued
     float* ws_s = reinterpret_cast<float*>(flags + 4);          // [2][kbs_max]
     float* as_s = ws_s + 2 * kbs_max;                           // [MT][kbs_max]
     uintptr_t act_addr = reinterpret_cast<uintptr_t>(as_s + MT * kbs_max);
     uint8_t* act = reinterpret_cast<uint8_t*>((act_addr + 15) & ~static_cast<uintptr_t>(15));
-    const int act_ld = (AMODE == A_BF16) ? (2 * kslice + 32) : (kslice + 16);
+    // Row stride of the activation slice.  W8A8 (fused): bf16 rows whose first
+    // kslice bytes are overwritten in place by the e4m3 codes; +16 keeps the
+    // code rows on distinct banks for the B-fragment loads.  Weight-only: bf16
+    // rows, +32 for the 8-byte B-fragment loads.  Unfused: e4m3 rows.
+    const int act_ld = (AMODE == A_QUANT) ? (2 * kslice + 16) : (AMODE == A_BF16) ? (2 * kslice + 32) : (kslice + 16);
+    const int row_bytes = (AMODE == A_PREQ) ? nkb * kBlock : 2 * nkb * kBlock;   // bytes copied per token
 
     if (tid == 0) {
 #pragma unroll
@@ -86,15 +94,17 @@ __global__ void __launch_bounds__(kStreamThreads)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCWarps);
         }
+        mbar_init(abar, 1);
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    // ---- producer prologue: fill the whole ring before anything else ----
+    // ---- producer prologue: fill the whole ring, then fetch the activations ----
     const int npro = min(nkb, kStages);
-    if (warp == kCWarps && lane == 0) {
+    const bool producer = (warp == kCWarps && lane == 0);
+    if (producer) {
         tma_prefetch_desc(&wmap);
         for (int i = 0; i < npro; ++i) {
             mbar_expect_tx(&full[i], kStageBytes);
@@ -106,57 +116,58 @@ __global__ void __launch_bounds__(kStreamThreads)
     // Weights never come from the preceding kernel; activations and scales may.
     pdl_trigger();
     pdl_wait();
+    if (producer) {
+        mbar_expect_tx(abar, (uint32_t)(mvalid * row_bytes));
+        for (int tok = 0; tok < mvalid; ++tok) {
+            const uint8_t* src = (AMODE == A_PREQ)
+                ? p.aq + (int64_t)(m0 + tok) * p.K + (int64_t)kb0 * kBlock
+                : reinterpret_cast<const uint8_t*>(p.a + (int64_t)(m0 + tok) * p.K + (int64_t)kb0 * kBlock);
+            bulk_load(act + tok * act_ld, src, (uint32_t)row_bytes, abar);
+        }
+    }
 
     for (int i = tid; i < nkb; i += kStreamThreads) {
         ws_s[i] = p.ws[(int64_t)nb0 * KB + kb0 + i];
         ws_s[kbs_max + i] = p.ws[(int64_t)nb1 * KB + kb0 + i];
     }
+    // rows past the last token: zero codes / activations and zero scales
+    for (int c = tid; c < (MT - mvalid) * (row_bytes / 16); c += kStreamThreads) {
+        const int tok = mvalid + c / (row_bytes / 16), ch = c % (row_bytes / 16);
+        *reinterpret_cast<uint4*>(act + tok * act_ld + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (AMODE != A_BF16) {
+        for (int c = tid; c < MT * nkb; c += kStreamThreads) {
+            const int tok = c / nkb, kbl = c - tok * nkb;
+            float v = 0.0f;
+            if (AMODE == A_PREQ && tok < mvalid) v = p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl];
+            as_s[tok * kbs_max + kbl] = v;
+        }
+    }
+    if (!mbar_wait(abar, 0)) {
+        record_error(p.err, kErrTimeout);
+        atomicExch(&flags[0], 1);
+    }
 
-    // ---- A-load ----
     if (AMODE == A_QUANT) {
-        const int ngroups = MT * nkb;
-        for (int gi = warp; gi < ngroups; gi += kCWarps + 1) {
-            const int tok = gi / nkb, kbl = gi - tok * nkb;
-            uint32_t codes = 0u;
-            float s = 0.0f;
-            if (tok < mvalid) {
-                const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + 4 * lane;
-                const uint2 v = *reinterpret_cast<const uint2*>(p.a + off);
-                codes = quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s);
+        // In-place group quantisation: one warp walks a token row's groups in
+        // increasing order, so the codes of group g (bytes [128g, 128g+128))
+        // only overwrite bf16 data of groups <= g that it has already read.
+        for (int tok = warp; tok < mvalid; tok += kCWarps + 1) {
+            uint8_t* row = act + tok * act_ld;
+            for (int kbl = 0; kbl < nkb; ++kbl) {
+                const uint2 v = *reinterpret_cast<const uint2*>(row + kbl * 2 * kBlock + 8 * lane);
+                float s;
+                const uint32_t codes =
+                    quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s);
+                __syncwarp();
+                *reinterpret_cast<uint32_t*>(row + kbl * kBlock + 4 * lane) = codes;
+                if (lane == 0) as_s[tok * kbs_max + kbl] = s;
                 if (p.aq != nullptr && tile == 0) {
+                    const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + 4 * lane;
                     *reinterpret_cast<uint32_t*>(p.aq + off) = codes;
                     if (lane == 0) p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] = s;
                 }
             }
-            *reinterpret_cast<uint32_t*>(act + tok * act_ld + kbl * kBlock + 4 * lane) = codes;
-            if (lane == 0) as_s[tok * kbs_max + kbl] = s;
-        }
-    } else if (AMODE == A_PREQ) {
-        const int chunks = nkb * (kBlock / 16);
-        for (int c = tid; c < MT * chunks; c += kStreamThreads) {
-            const int tok = c / chunks, ch = c - tok * chunks;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (tok < mvalid)
-                v = *reinterpret_cast<const uint4*>(p.aq + (int64_t)(m0 + tok) * p.K + (int64_t)kb0 * kBlock + ch * 16);
-            *reinterpret_cast<uint4*>(act + tok * act_ld + ch * 16) = v;
-        }
-        for (int c = tid; c < MT * nkb; c += kStreamThreads) {
-            const int tok = c / nkb, kbl = c - tok * nkb;
-            as_s[tok * kbs_max + kbl] = (tok < mvalid) ? p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] : 0.0f;
-        }
-    } else {
-        const int chunks = nkb * (kBlock / 8);       // 16-byte chunks (8 bf16)
-        for (int c = tid; c < MT * chunks; c += kStreamThreads) {
-            const int tok = c / chunks, ch = c - tok * chunks;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (tok < mvalid)
-                v = *reinterpret_cast<const uint4*>(p.a + (int64_t)(m0 + tok) * p.K + (int64_t)kb0 * kBlock + ch * 8);
-            uint4 o;
-            o.x = __byte_perm(v.x, v.y, 0x5410);     // (x0, x2)
-            o.y = __byte_perm(v.x, v.y, 0x7632);     // (x1, x3)
-            o.z = __byte_perm(v.z, v.w, 0x5410);
-            o.w = __byte_perm(v.z, v.w, 0x7632);
-            *reinterpret_cast<uint4*>(act + tok * act_ld + ch * 16) = o;
         }
     }
     __syncthreads();
@@ -218,12 +229,15 @@ __global__ void __launch_bounds__(kStreamThreads)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint8_t* bp = act + (nt * 8 + g) * act_ld + 2 * (i * kBlock + ks * 32 + 4 * t);
-                        const uint2 b = *reinterpret_cast<const uint2*>(bp);
-                        const uint2 c = *reinterpret_cast<const uint2*>(bp + 32);
+                        // (x0,x1),(x2,x3) -> (x0,x2),(x1,x3): the pairing of e4m3x4_to_bf16x2x2
+                        const uint2 bv = *reinterpret_cast<const uint2*>(bp);
+                        const uint2 cv = *reinterpret_cast<const uint2*>(bp + 32);
+                        const uint32_t b0 = __byte_perm(bv.x, bv.y, 0x5410), b1 = __byte_perm(bv.x, bv.y, 0x7632);
+                        const uint32_t c0 = __byte_perm(cv.x, cv.y, 0x5410), c1 = __byte_perm(cv.x, cv.y, 0x7632);
 #pragma unroll
                         for (int mt = 0; mt < 2; ++mt) {
-                            mma_bf16_16816(d[mt][nt], ev[mt][0], ev[mt][1], od[mt][0], od[mt][1], b.x, b.y);
-                            mma_bf16_16816(d[mt][nt], ev[mt][2], ev[mt][3], od[mt][2], od[mt][3], c.x, c.y);
+                            mma_bf16_16816(d[mt][nt], ev[mt][0], ev[mt][1], od[mt][0], od[mt][1], b0, b1);
+                            mma_bf16_16816(d[mt][nt], ev[mt][2], ev[mt][3], od[mt][2], od[mt][3], c0, c1);
                         }
                     }
                 }

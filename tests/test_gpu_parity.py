@@ -82,6 +82,36 @@ def test_quant_group128_bit_exact(r9q, M, K, p, factor, seed):
     assert np.array_equal(xq.cpu().numpy(), oq)
 
 
+def test_quant_quotient_every_bf16_value(r9q):
+    """The quantiser's division-free quotient against the oracle's fp32 division:
+    every finite bf16 magnitude x, both signs, against 600 group maxima (random
+    bf16 values plus subnormal, tiny and huge ones), as groups [amax, x...]."""
+    rng = np.random.default_rng(77)
+    all_pos = np.arange(0, 0x7F80, dtype=np.uint16)                    # finite non-negative bf16
+    amaxes = np.concatenate([rng.integers(0x0001, 0x7F80, 590).astype(np.uint16),
+                             np.uint16([0x0001, 0x0040, 0x0080, 0x0100, 0x0C00, 0x3F80, 0x43E0, 0x7F7F,
+                                        0x7F00, 0x0200])])
+    xs_all = f32_of_bits(all_pos)
+    groups = []
+    for a in amaxes:
+        av = f32_of_bits(np.uint16([a]))[0]
+        cand = all_pos[xs_all <= av]
+        cand = cand[rng.permutation(cand.size)[:4064]]                  # up to 32 groups per amax
+        cand = cand | (rng.integers(0, 2, cand.size).astype(np.uint16) << 15)   # random signs
+        pad = (-cand.size) % 127
+        cand = np.concatenate([cand, np.zeros(pad, np.uint16)]).reshape(-1, 127)
+        groups.append(np.concatenate([np.full((cand.shape[0], 1), a, np.uint16), cand], axis=1))
+    flat = np.concatenate(groups)
+    flat = np.concatenate([flat, np.zeros(((-flat.shape[0]) % 8, 128), np.uint16)])
+    xb = flat.reshape(-1, 1024)
+    xq, xs = r9q.r9q_quant_group128(bf16_to_dev(xb))
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_group(xb)
+    assert np.array_equal(xs.cpu().numpy(), os_)
+    bad = np.nonzero(xq.cpu().numpy() != oq)
+    assert bad[0].size == 0, (bad[0][:5], bad[1][:5])
+
+
 def test_weight_block_quant_bit_exact(r9q):
     quantised_weights(r9q, 0, 512, 1024)
     quantised_weights(r9q, 1, 4096, 4096)
