@@ -147,7 +147,11 @@ size_t stream_smem_bytes(int MT, int amode, int kbs_max) {
     return 1024 + off + (size_t)MT * act_ld;
 }
 
-bool plan_stream(int64_t M, int64_t N, int64_t K, int amode, int sms, StreamPlan* plan) {
+bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, StreamPlan* plan) {
+    // The split count fixes the fp32 summation order.  Fused (A_QUANT) and
+    // unfused (A_PREQ) W8A8 calls must sum identically, so both are planned
+    // with the fused A-load's shared-memory needs.
+    const int amode = (amode_launch == A_PREQ) ? A_QUANT : amode_launch;
     const int MT = M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
     const int ntiles = (int)(N / 128);
     const int mchunks = (int)((M + MT - 1) / MT);
@@ -180,7 +184,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode, int sms, StreamPlan
     plan->splits = best;
     plan->ntiles = ntiles;
     plan->mchunks = mchunks;
-    plan->smem = stream_smem_bytes(MT, amode, (KB + best - 1) / best);
+    plan->smem = stream_smem_bytes(MT, amode_launch, (KB + best - 1) / best);
     return true;
 }
 
