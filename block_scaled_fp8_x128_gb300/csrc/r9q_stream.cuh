@@ -135,13 +135,16 @@ __global__ void __launch_bounds__(kStreamThreads)
         const int tok = mvalid + c / (row_bytes / 16), ch = c % (row_bytes / 16);
         *reinterpret_cast<uint4*>(act + tok * act_ld + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (AMODE != A_BF16) {
+    if (AMODE == A_PREQ) {
         for (int c = tid; c < MT * nkb; c += kStreamThreads) {
             const int tok = c / nkb, kbl = c - tok * nkb;
-            float v = 0.0f;
-            if (AMODE == A_PREQ && tok < mvalid) v = p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl];
-            as_s[tok * kbs_max + kbl] = v;
+            as_s[tok * kbs_max + kbl] = (tok < mvalid) ? p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] : 0.0f;
         }
+    } else if (AMODE == A_QUANT) {
+        // only the padding rows: the scales of rows < mvalid are written by the
+        // quant loop below, which other warps may already be running
+        for (int c = tid; c < (MT - mvalid) * nkb; c += kStreamThreads)
+            as_s[(mvalid + c / nkb) * kbs_max + c % nkb] = 0.0f;
     }
     if (!mbar_wait(abar, 0)) {
         record_error(p.err, kErrTimeout);
