@@ -139,10 +139,11 @@ size_t mlp_workspace(int64_t M, int64_t I, int flags, bool have_h, bool have_hq)
 
 // ------------------------------------------------------------ planning --
 
-size_t stream_smem_bytes(int MT, int amode, int kbs_max) {
+size_t stream_smem_bytes(int MT, int amode, int kbs_max, int ntl_max, int stages) {
     const size_t kslice = (size_t)kbs_max * 128;
     const size_t act_ld = (amode == A_QUANT) ? 2 * kslice + 16 : (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16;
-    size_t off = (size_t)kStages * kStageBytes + 16 * kStages + 16 + 16 + 4 * (2 * (size_t)kbs_max + (size_t)MT * kbs_max);
+    size_t off = (size_t)stages * kStageBytes + kBarBytes + 2 * (size_t)MT * kPStride * 4 +
+                 4 * ((size_t)ntl_max * 2 * kbs_max + (size_t)MT * kbs_max);
     off = (off + 15) & ~static_cast<size_t>(15);
     return 1024 + off + (size_t)MT * act_ld;
 }
@@ -158,33 +159,58 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
     const int KB = (int)(K / 128);
     const int maxS = KB < 8 ? KB : 8;
     const int per_sm_cap = MT >= 64 ? 1 : MT >= 32 ? 2 : 3;   // register-limited residency
-    int best = -1;
     const int forced = env_splits();
-    if (forced >= 1 && forced <= maxS && stream_smem_bytes(MT, amode, (KB + forced - 1) / forced) <= kSmemLimit)
-        best = forced;
-    if (best < 0) {
-        // largest divisor of KB whose CTAs are all co-resident
-        for (int S = 1; S <= maxS; ++S) {
-            if (KB % S) continue;
-            const size_t smem = stream_smem_bytes(MT, amode, KB / S);
-            if (smem > kSmemLimit) continue;
-            int per_sm = (int)((228 * 1024) / (smem + 1024));
-            if (per_sm > per_sm_cap) per_sm = per_sm_cap;
-            const int64_t ctas = (int64_t)ntiles * mchunks * S;
-            if (ctas <= (int64_t)sms * per_sm) best = S;
+    // Candidates: S | KB (S <= 8), G | ntiles, ring depth 4..2.  Keep every CTA
+    // co-resident; among those take the most CTAs (up to two per SM), then
+    // the deeper ring, then fewer splits.
+    int bS = -1, bG = -1, bst = -1;
+    long best_score = -1;
+    for (int S = 1; S <= maxS; ++S) {
+        if (KB % S) continue;
+        if (forced && S != forced) continue;
+        for (int G = 1; G <= ntiles; ++G) {
+            if (ntiles % G) continue;
+            const int ntl_max = ntiles / G;
+            for (int st = kMaxStages; st >= 2; --st) {
+                const size_t smem = stream_smem_bytes(MT, amode, KB / S, ntl_max, st);
+                if (smem > kSmemLimit) continue;
+                int per_sm = (int)((228 * 1024) / (smem + 1024));
+                if (per_sm > per_sm_cap) per_sm = per_sm_cap;
+                const int64_t ctas = (int64_t)S * G * mchunks;
+                if (ctas > (int64_t)sms * per_sm) continue;
+                const int64_t useful = ctas < 2 * (int64_t)sms ? ctas : 2 * (int64_t)sms;
+                const long score = (long)useful * 64 + st * 8 - S;
+                if (score > best_score) {
+                    best_score = score;
+                    bS = S;
+                    bG = G;
+                    bst = st;
+                }
+                break;   // deepest ring that fits for this (S, G)
+            }
         }
     }
-    if (best < 0) {
-        // nothing is co-resident: the smallest split whose shared memory fits
-        for (int S = 1; S <= maxS && best < 0; ++S)
-            if (stream_smem_bytes(MT, amode, (KB + S - 1) / S) <= kSmemLimit) best = S;
+    if (bS < 0) {
+        // not co-resident at any split: one tile per cluster, the smallest split that fits
+        for (int S = 1; S <= maxS && bS < 0; ++S) {
+            if (KB % S) continue;
+            for (int st = kMaxStages; st >= 2; --st)
+                if (stream_smem_bytes(MT, amode, KB / S, 1, st) <= kSmemLimit) {
+                    bS = S;
+                    bG = ntiles;
+                    bst = st;
+                    break;
+                }
+        }
     }
-    if (best < 0) return false;
+    if (bS < 0) return false;
     plan->MT = MT;
-    plan->splits = best;
+    plan->splits = bS;
+    plan->groups = bG;
     plan->ntiles = ntiles;
     plan->mchunks = mchunks;
-    plan->smem = stream_smem_bytes(MT, amode_launch, (KB + best - 1) / best);
+    plan->stages = bst;
+    plan->smem = stream_smem_bytes(MT, amode_launch, KB / bS, (ntiles + bG - 1) / bG, bst);
     return true;
 }
 
@@ -234,6 +260,9 @@ int run_stream_gemm(int amode, int epi, const void* a, uint8_t* aq, float* as, c
     p.KB = (int)(K / 128);
     p.ldy = (int)ldy;
     p.splits = plan.splits;
+    p.groups = plan.groups;
+    p.ntiles = plan.ntiles;
+    p.stages = plan.stages;
     p.err = d->err;
     return to_status(launch_stream(plan, amode, epi, tm, p, st, pdl));
 }

@@ -12,11 +12,12 @@ namespace r9q {
 enum AMode : int { A_QUANT = 0, A_PREQ = 1, A_BF16 = 2 };
 enum Epi : int { EPI_STORE = 0, EPI_SWIGLU = 1 };
 
-constexpr int kStages = 4;                       // weight ring depth
-constexpr int kCWarps = 4;                       // consumer (MMA) warps
+constexpr int kMaxStages = 4;                    // weight ring depth (runtime 2..4)
+constexpr int kCWarps = 8;                       // consumer (MMA) warps, 16 weight rows each
 constexpr int kStreamThreads = (kCWarps + 1) * 32;
 constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m3)
 constexpr int kPStride = 128 + 4;                // fp32 partial row stride (floats)
+constexpr int kBarBytes = 256;                   // mbarriers + flags
 
 struct StreamParams {
     const uint16_t* a;   // bf16 activations [M][K]          (A_QUANT, A_BF16)
@@ -25,19 +26,24 @@ struct StreamParams {
     const float* ws;     // fp32 [NB][KB] weight block scales
     uint16_t* y;         // bf16 output [M][ldy] (EPI_STORE: y, EPI_SWIGLU: h)
     int M, K, KB, ldy;
-    int splits;          // K splits = cluster size
+    int splits;          // K splits = cluster size S
+    int groups;          // tile groups G: cluster g owns tiles g, g+G, ...
+    int ntiles;          // 128-row weight tiles
+    int stages;          // ring depth
     int* err;            // device error word
 };
 
 struct StreamPlan {
     int MT;              // token tile: 8, 16, 32 or 64
     int splits;          // cluster size along K
+    int groups;          // tile groups
     int ntiles;          // 128-row weight tiles
     int mchunks;         // ceil(M / MT)
+    int stages;          // ring depth
     size_t smem;         // dynamic shared memory bytes
 };
 
-size_t stream_smem_bytes(int MT, int amode, int kbs_max);
+size_t stream_smem_bytes(int MT, int amode, int kbs_max, int ntl_max, int stages);
 // Chooses MT and the split count; returns false when no configuration fits.
 bool plan_stream(int64_t M, int64_t N, int64_t K, int amode, int sms, StreamPlan* plan);
 
