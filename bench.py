@@ -182,6 +182,10 @@ def run_gpu(args):
     bpc = gemm_bytes(M, N, K_)
     copies = _copies_for(bpc)
     X, W, S, Y = _make_inputs(torch, r9q, "w8bf16", M, N, K_, 1, 0.0, 1.0, copies, dev)
+    torch.cuda.synchronize()
+    # decode-step launch mode: weights are constant, so each GEMM may start
+    # streaming them while the previous call finishes (include/r9q.h, r9q_set_pdl)
+    r9q.r9q_set_pdl(not args.no_pdl)
 
     def step(i):
         r9q.r9q_gemm_fp8w_bf16a(X[i], W[i], S[i], y=Y[i])
@@ -232,7 +236,8 @@ def run_gpu(args):
         "config": {"workload": "weight-only fp8 decode GEMM M=16 N=4096 K=4096 (seed 1)",
                    "M": M, "N": N, "K": K_, "bytes_per_call": bpc,
                    "l2": f"rotating {copies} weight/activation copies ({copies * bpc / 1e6:.0f} MB > 129 MB L2)",
-                   "timing": "CUDA-graph replay of exactly K calls, CUDA events on the replay stream"},
+                   "timing": "CUDA-graph replay of exactly K calls, CUDA events on the replay stream",
+                   "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4), "traffic": None,
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback"},
@@ -272,6 +277,7 @@ def sweep(torch, r9q, stream, hbm, fp8_peak, src):
         bpc = gemm_bytes(M, N, K)
         copies = min(_copies_for(bpc), 64)
         X, W, S, Y = _make_inputs(torch, r9q, kind, M, N, K, seed, p, fac, copies, dev)
+        torch.cuda.synchronize()
 
         def fn(i):
             r9q.r9q_gemm_fp8_block_qa(X[i], W[i], S[i], y=Y[i])
@@ -297,6 +303,7 @@ def sweep(torch, r9q, stream, hbm, fp8_peak, src):
     WD = [wdn.clone() for _ in range(copies)]
     HB = [torch.empty((M, I), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
     YB = [torch.empty((M, Ho), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+    torch.cuda.synchronize()
     for flags, label in ((0, "fused"), (r9q.R9Q_MLP_UNFUSED, "separate launches")):
         ws_b = r9q.r9q_workspace_bytes(r9q.R9Q_OP_GATE_UP_SWIGLU_DOWN, M, I, H, Ho, flags)
         wsp = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
@@ -371,6 +378,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-pdl", action="store_true", help="launch every GEMM fully serialised")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

@@ -29,6 +29,7 @@ _SIGS = {
     "r9q_version": ([], ctypes.c_int),
     "r9q_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "r9q_last_device_error": ([_P], ctypes.c_int),
+    "r9q_set_pdl": ([ctypes.c_int], ctypes.c_int),
     "r9q_e4m3_from_f32": ([_P, _I64, _P, _P], ctypes.c_int),
     "r9q_quant_group128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "r9q_quant_weight_block128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
@@ -94,6 +95,11 @@ def r9q_version() -> int:
 
 def r9q_strerror(code: int) -> str:
     return _lib.r9q_strerror(int(code)).decode()
+
+
+def r9q_set_pdl(enable: bool) -> bool:
+    """Programmatic dependent launch for the GEMMs (see include/r9q.h); returns the previous setting."""
+    return bool(_lib.r9q_set_pdl(int(bool(enable))))
 
 
 def r9q_last_device_error(stream=None) -> int:

@@ -114,6 +114,8 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? R9Q_OK : R9Q_ERR_LAUNCH
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+std::atomic<int> g_pdl{0};
+
 int env_splits() {
     static int v = -1;
     if (v < 0) {
@@ -276,6 +278,8 @@ extern "C" {
 
 int r9q_version(void) { return R9Q_VERSION; }
 
+int r9q_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
 const char* r9q_strerror(int code) {
     switch (code) {
         case R9Q_OK: return "ok";
@@ -389,7 +393,7 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     rc = current_device(&d);
     if (rc) return rc;
     return run_stream_gemm(a_bf16 ? A_QUANT : A_PREQ, EPI_STORE, a_bf16, aq, as, w, ws, y_bf16, N, M, N, K, d,
-                           static_cast<cudaStream_t>(stream), false);
+                           static_cast<cudaStream_t>(stream), g_pdl.load() != 0);
 }
 
 int r9q_gemm_fp8w_bf16a(const void* a_bf16, const uint8_t* w, const float* ws, void* y_bf16, int64_t M,
@@ -407,7 +411,7 @@ int r9q_gemm_fp8w_bf16a(const void* a_bf16, const uint8_t* w, const float* ws, v
     rc = current_device(&d);
     if (rc) return rc;
     return run_stream_gemm(A_BF16, EPI_STORE, a_bf16, nullptr, nullptr, w, ws, y_bf16, N, M, N, K, d,
-                           static_cast<cudaStream_t>(stream), false);
+                           static_cast<cudaStream_t>(stream), g_pdl.load() != 0);
 }
 
 int r9q_gate_up_swiglu_down(const void* x_bf16, const uint8_t* w_gu, const float* s_gu, const uint8_t* w_dn,
@@ -462,7 +466,8 @@ int r9q_gate_up_swiglu_down(const void* x_bf16, const uint8_t* w_gu, const float
 
     const int amode = wonly ? A_BF16 : A_QUANT;
     if (!unfused) {
-        rc = run_stream_gemm(amode, EPI_SWIGLU, x_bf16, nullptr, nullptr, w_gu, s_gu, h, I, M, 2 * I, H, d, st, false);
+        rc = run_stream_gemm(amode, EPI_SWIGLU, x_bf16, nullptr, nullptr, w_gu, s_gu, h, I, M, 2 * I, H, d, st,
+                             g_pdl.load() != 0);
         if (rc) return rc;
         // the down GEMM streams its weights while the gate_up GEMM finishes (programmatic launch)
         return run_stream_gemm(amode, EPI_STORE, h, hq, hs, w_dn, s_dn, y_bf16, H_out, M, H_out, I, d, st, true);

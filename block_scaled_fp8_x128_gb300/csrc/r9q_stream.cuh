@@ -50,7 +50,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
             : "r"(smem_u32(bar)), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (i >= 8) __nanosleep(64);
     }
     return false;
 }
@@ -137,8 +136,10 @@ __global__ void __launch_bounds__(kStreamThreads)
         flags[1] = 0;
         fence_mbar_init();
     }
-    // every peer's barriers must exist before anyone arrives on them remotely
-    cluster_sync();
+    // Every peer's barriers must exist before anyone arrives on them remotely:
+    // arrive on the cluster barrier now, wait for it only just before the
+    // first remote arrive, so the weight stream starts at once.
+    cluster_arrive();
 
     // ---- producer prologue: fill the ring, then fetch the activations ----
     const bool producer = (warp == kCWarps && lane == 0);
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kStreamThreads)
 
     const int g = lane >> 2, t = lane & 3;
     if (warp < kCWarps) {
+        cluster_wait();
         // ---- MMA warps: rows [16*warp, 16*warp + 16) of every tile ----
         const int box = warp >> 2;
         const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -360,7 +362,10 @@ __global__ void __launch_bounds__(kStreamThreads)
             if (tid == 0)
                 for (int r = 0; r < S; ++r) mbar_arrive_remote(&pfree[b], (uint32_t)r);
         }
-    } else if (lane == 0) {
+    } else {
+        cluster_wait();
+    }
+    if (warp == kCWarps && lane == 0) {
         // ---- producer steady state (runs ahead across tiles) ----
         int issued = npro;
         int cur_tl = -1, r0 = 0, r1 = 0, nb0, nb1;

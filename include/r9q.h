@@ -70,6 +70,17 @@ const char* r9q_strerror(int code);
  * otherwise the recorded negative code (R9Q_ERR_TIMEOUT). */
 int r9q_last_device_error(void* stream);
 
+/* Programmatic dependent launch of the GEMM entry points (default: off).
+ * When on, a GEMM kernel may begin while the kernel launched just before it on
+ * the same stream is still running: it starts streaming its weights w at once
+ * and waits for that kernel to finish before it reads anything else
+ * (activations, scales) or writes anything.  Turn it on only where the kernel
+ * launched immediately before each GEMM never writes that GEMM's weights (a
+ * decode step: the weights are constant).  Process-wide; returns the previous
+ * setting.  The down GEMM inside r9q_gate_up_swiglu_down always uses it (its
+ * predecessor is the library's own gate_up kernel). */
+int r9q_set_pdl(int enable);
+
 /* fp32 -> e4m3 conversion used by every quantiser: round to nearest even,
  * saturating to +-448 (OCP FP8 E4M3; the saturation rule of the operation's
  * statement).  x: n floats, q: n bytes.  n >= 0 (0 is a no-op). */

@@ -307,3 +307,27 @@ def test_graph_replay_alternating_shapes(r9q):
 
 def test_device_error_word_clear(r9q):
     assert r9q.r9q_last_device_error() == 0
+
+
+def test_pdl_dependent_chain_matches_serialised(r9q):
+    """With programmatic launch on, a GEMM whose activations are the previous
+    GEMM's output must still see that output: a 6-deep chain, PDL on vs off."""
+    K = 1024
+    ws_list = [quantised_weights(r9q, 20 + i, K, K, check_oracle=False) for i in range(6)]
+    x = bf16_to_dev(activations_bf16(21, 16, K))
+    outs = {}
+    for pdl in (False, True):
+        prev = r9q.r9q_set_pdl(pdl)
+        try:
+            h = x
+            for i, (wq, ws) in enumerate(ws_list):
+                if i % 2:
+                    h = r9q.r9q_gemm_fp8w_bf16a(h, wq, ws)
+                else:
+                    h = r9q.r9q_gemm_fp8_block_qa(h, wq, ws)
+            torch.cuda.synchronize()
+            outs[pdl] = h.clone()
+        finally:
+            r9q.r9q_set_pdl(prev)
+    assert torch.equal(outs[False].view(torch.int16), outs[True].view(torch.int16))
+    assert r9q.r9q_last_device_error() == 0
