@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(kStreamThreads)
         flags[1] = 0;
         fence_mbar_init();
     }
+    // the producer and the MMA warps use the barriers thread 0 just initialised
+    __syncthreads();
     // Every peer's barriers must exist before anyone arrives on them remotely:
     // arrive on the cluster barrier now, wait for it only just before the
     // first remote arrive, so the weight stream starts at once.
