@@ -54,9 +54,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     return false;
 }
 
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
-    const uint32_t addr = dsmem_addr(smem_u32(local_bar), rank);
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+// Arrive on the barrier at the same shared-memory offset in every CTA of the
+// cluster.  One cluster-scope fence releases everything this CTA did before
+// (the caller synchronises the CTA's writers first); the arrives themselves
+// are relaxed, so the release is paid once rather than once per peer.
+__device__ __forceinline__ void mbar_arrive_all_ranks(uint64_t* local_bar, int S) {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    const uint32_t a = smem_u32(local_bar);
+    for (int r = 0; r < S; ++r) {
+        const uint32_t addr = dsmem_addr(a, (uint32_t)r);
+        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+    }
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -128,15 +136,18 @@ __global__ void __launch_bounds__(kStreamThreads)
             mbar_init(&empty[s], kCWarps);
         }
         mbar_init(abar, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_proxy_async_smem();     // the TMA unit sees the initialised ring barriers
+    }
+    if (tid == 32) {
         mbar_init(&pfull[0], S);
         mbar_init(&pfull[1], S);
         mbar_init(&pfree[0], S);
         mbar_init(&pfree[1], S);
-        flags[0] = 0;
-        flags[1] = 0;
-        fence_mbar_init();
+        fence_mbar_init();            // peers see them once the cluster barrier below completes
     }
-    // the producer and the MMA warps use the barriers thread 0 just initialised
+    // the producer and the MMA warps use the barriers just initialised
     __syncthreads();
     // Every peer's barriers must exist before anyone arrives on them remotely:
     // arrive on the cluster barrier now, wait for it only just before the
@@ -319,16 +330,23 @@ __global__ void __launch_bounds__(kStreamThreads)
                 Pb[(tok + 1) * kPStride + r + 8] = acc[nt][3];
             }
             consumer_sync();
-            if (tid == 0)
-                for (int r = 0; r < S; ++r) mbar_arrive_remote(&pfull[b], (uint32_t)r);
+            if (tid == 0) mbar_arrive_all_ranks(&pfull[b], S);
             if (*vflags == 0 && !mbar_wait_cluster(&pfull[b], use & 1u)) fail();
 
             // ---- split-K reduction of slice `split` over ranks 0..S-1 + epilogue ----
+            // Sums go to registers first; the peers are told their partials are
+            // free before the global stores, so the release never waits on them.
             const uint32_t pbase = smem_u32(Pb);
             constexpr int UPT = (EPI == EPI_SWIGLU) ? 32 : 64;   // units per token
+            constexpr int MAXU = (MT * UPT + kCWarps * 32 - 1) / (kCWarps * 32);   // units per thread, S = 1
             const int U = MT * UPT;
             const int u_lo = (split * U) / S, u_hi = ((split + 1) * U) / S;
-            for (int u = u_lo + tid; u < u_hi; u += kCWarps * 32) {
+            uint32_t outv[MAXU];
+#pragma unroll
+            for (int j = 0; j < MAXU; ++j) {
+                const int u = u_lo + tid + j * kCWarps * 32;
+                outv[j] = 0u;
+                if (u >= u_hi) continue;
                 const int tok = u / UPT, up = u - tok * UPT;
                 if (tok >= mvalid) continue;
                 if (EPI == EPI_STORE) {
@@ -339,8 +357,7 @@ __global__ void __launch_bounds__(kStreamThreads)
                         sum.x = __fadd_rn(sum.x, v.x);
                         sum.y = __fadd_rn(sum.y, v.y);
                     }
-                    *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + kBlock * tile + 2 * up) =
-                        pack_bf16x2(sum.x, sum.y);
+                    outv[j] = pack_bf16x2(sum.x, sum.y);
                 } else {
                     const uint32_t offg = (uint32_t)((tok * kPStride + 2 * up) * 4);
                     const uint32_t offu = offg + 64 * 4;
@@ -356,13 +373,27 @@ __global__ void __launch_bounds__(kStreamThreads)
                     }
                     const float h0 = silu_mul(bf16_round(gs.x), bf16_round(us.x));
                     const float h1 = silu_mul(bf16_round(gs.y), bf16_round(us.y));
-                    *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + 64 * tile + 2 * up) =
-                        pack_bf16x2(h0, h1);
+                    outv[j] = pack_bf16x2(h0, h1);
                 }
             }
             consumer_sync();
-            if (tid == 0)
-                for (int r = 0; r < S; ++r) mbar_arrive_remote(&pfree[b], (uint32_t)r);
+            if (tid == 0) mbar_arrive_all_ranks(&pfree[b], S);
+#pragma unroll
+            for (int j = 0; j < MAXU; ++j) {
+                const int u = u_lo + tid + j * kCWarps * 32;
+                if (u >= u_hi) continue;
+                const int tok = u / UPT, up = u - tok * UPT;
+                if (tok >= mvalid) continue;
+                const int64_t col = (EPI == EPI_STORE) ? (int64_t)kBlock * tile + 2 * up : (int64_t)64 * tile + 2 * up;
+                *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + col) = outv[j];
+            }
+        }
+        // Peers stop touching this CTA's shared memory once every rank has
+        // arrived on its pfree barriers for their last use: wait for those
+        // instead of a cluster-wide barrier at exit.
+        for (int b2 = 0; b2 < 2 && b2 < ntl; ++b2) {
+            const uint32_t last_use = (uint32_t)((ntl - 1 - b2) >> 1);
+            if (!mbar_wait_cluster(&pfree[b2], last_use & 1u)) fail();   // also after an error
         }
     } else {
         cluster_wait();
@@ -399,8 +430,6 @@ __global__ void __launch_bounds__(kStreamThreads)
         for (int it = max(0, issued - nst); it < issued; ++it)
             (void)mbar_wait(&full[it % nst], (uint32_t)(it / nst) & 1u);
     }
-    // keep every CTA's shared memory alive until all peers have finished with it
-    cluster_sync();
 }
 
 template <int AMODE>
