@@ -144,7 +144,8 @@ size_t mlp_workspace(int64_t M, int64_t I, int flags, bool have_h, bool have_hq)
 size_t stream_smem_bytes(int MT, int amode, int kbs_max, int ntl_max, int stages) {
     const size_t kslice = (size_t)kbs_max * 128;
     const size_t act_ld = (amode == A_QUANT) ? 2 * kslice + 16 : (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16;
-    size_t off = (size_t)stages * kStageBytes + kBarBytes + 2 * (size_t)MT * kPStride * 4 +
+    const size_t npbuf = ntl_max > 1 ? 2 : 1;
+    size_t off = (size_t)stages * kStageBytes + kBarBytes + npbuf * (size_t)MT * kPStride * 4 +
                  4 * ((size_t)ntl_max * 2 * kbs_max + (size_t)MT * kbs_max);
     off = (off + 15) & ~static_cast<size_t>(15);
     return 1024 + off + (size_t)MT * act_ld;
@@ -159,7 +160,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
     const int ntiles = (int)(N / 128);
     const int mchunks = (int)((M + MT - 1) / MT);
     const int KB = (int)(K / 128);
-    const int maxS = KB < 8 ? KB : 8;
+    const int maxS = KB < kMaxSplits ? KB : kMaxSplits;
     const int per_sm_cap = MT >= 64 ? 1 : MT >= 32 ? 2 : 3;   // register-limited residency
     const int forced = env_splits();
     // Candidates: S | KB (S <= 8), G | ntiles, ring depth 4..2.  Keep every CTA

@@ -18,6 +18,7 @@ constexpr int kStreamThreads = (kCWarps + 1) * 32;
 constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m3)
 constexpr int kPStride = 128 + 4;                // fp32 partial row stride (floats)
 constexpr int kBarBytes = 256;                   // mbarriers + flags
+constexpr int kMaxSplits = 8;                    // cluster size limit (portable)
 
 struct StreamParams {
     const uint16_t* a;   // bf16 activations [M][K]          (A_QUANT, A_BF16)

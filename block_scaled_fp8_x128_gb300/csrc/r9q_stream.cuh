@@ -118,8 +118,9 @@ __global__ void __launch_bounds__(kStreamThreads)
     uint64_t* pfull = abar + 1;                  // [2] every rank's partial is parked
     uint64_t* pfree = abar + 3;                  // [2] every rank has read my partial
     int* flags = reinterpret_cast<int*>(bars + 2 * kMaxStages + 5);   // [0] error, [1] issued
-    float* P = reinterpret_cast<float*>(smem + nst * kStageBytes + kBarBytes);   // [2][MT][kPStride]
-    float* ws_s = P + 2 * MT * kPStride;                              // [ntl_max][2][kbs_max]
+    float* P = reinterpret_cast<float*>(smem + nst * kStageBytes + kBarBytes);   // [npbuf][MT][kPStride]
+    const int npbuf = ntl_max > 1 ? 2 : 1;                            // partial buffers
+    float* ws_s = P + npbuf * MT * kPStride;                          // [ntl_max][2][kbs_max]
     float* as_s = ws_s + ntl_max * 2 * kbs_max;                       // [MT][kbs_max]
     uintptr_t act_addr = reinterpret_cast<uintptr_t>(as_s + MT * kbs_max);
     uint8_t* act = reinterpret_cast<uint8_t*>((act_addr + 15) & ~static_cast<uintptr_t>(15));
@@ -349,28 +350,41 @@ __global__ void __launch_bounds__(kStreamThreads)
                 if (u >= u_hi) continue;
                 const int tok = u / UPT, up = u - tok * UPT;
                 if (tok >= mvalid) continue;
+                // all ranks' partials are loaded first (independent remote
+                // loads in flight together), then summed in rank order
                 if (EPI == EPI_STORE) {
                     const uint32_t off = (uint32_t)((tok * kPStride + 2 * up) * 4);
-                    float2 sum = ld_dsmem_f32x2(dsmem_addr(pbase + off, 0));
-                    for (int r = 1; r < S; ++r) {
-                        const float2 v = ld_dsmem_f32x2(dsmem_addr(pbase + off, (uint32_t)r));
-                        sum.x = __fadd_rn(sum.x, v.x);
-                        sum.y = __fadd_rn(sum.y, v.y);
-                    }
+                    float2 v[kMaxSplits];
+#pragma unroll
+                    for (int r = 0; r < kMaxSplits; ++r)
+                        if (r < S) v[r] = ld_dsmem_f32x2(dsmem_addr(pbase + off, (uint32_t)r));
+                    float2 sum = v[0];
+#pragma unroll
+                    for (int r = 1; r < kMaxSplits; ++r)
+                        if (r < S) {
+                            sum.x = __fadd_rn(sum.x, v[r].x);
+                            sum.y = __fadd_rn(sum.y, v[r].y);
+                        }
                     outv[j] = pack_bf16x2(sum.x, sum.y);
                 } else {
                     const uint32_t offg = (uint32_t)((tok * kPStride + 2 * up) * 4);
                     const uint32_t offu = offg + 64 * 4;
-                    float2 gs = ld_dsmem_f32x2(dsmem_addr(pbase + offg, 0));
-                    float2 us = ld_dsmem_f32x2(dsmem_addr(pbase + offu, 0));
-                    for (int r = 1; r < S; ++r) {
-                        const float2 gv = ld_dsmem_f32x2(dsmem_addr(pbase + offg, (uint32_t)r));
-                        const float2 uv = ld_dsmem_f32x2(dsmem_addr(pbase + offu, (uint32_t)r));
-                        gs.x = __fadd_rn(gs.x, gv.x);
-                        gs.y = __fadd_rn(gs.y, gv.y);
-                        us.x = __fadd_rn(us.x, uv.x);
-                        us.y = __fadd_rn(us.y, uv.y);
-                    }
+                    float2 gv[kMaxSplits], uv[kMaxSplits];
+#pragma unroll
+                    for (int r = 0; r < kMaxSplits; ++r)
+                        if (r < S) {
+                            gv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offg, (uint32_t)r));
+                            uv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offu, (uint32_t)r));
+                        }
+                    float2 gs = gv[0], us = uv[0];
+#pragma unroll
+                    for (int r = 1; r < kMaxSplits; ++r)
+                        if (r < S) {
+                            gs.x = __fadd_rn(gs.x, gv[r].x);
+                            gs.y = __fadd_rn(gs.y, gv[r].y);
+                            us.x = __fadd_rn(us.x, uv[r].x);
+                            us.y = __fadd_rn(us.y, uv[r].y);
+                        }
                     const float h0 = silu_mul(bf16_round(gs.x), bf16_round(us.x));
                     const float h1 = silu_mul(bf16_round(gs.y), bf16_round(us.y));
                     outv[j] = pack_bf16x2(h0, h1);
