@@ -63,6 +63,8 @@ int current_device(DeviceInfo** out) {
     return d.status;
 }
 
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -96,6 +98,32 @@ int weight_tmap(const uint8_t* w, int64_t N, int64_t K, CUtensorMap* tm) {
     return r == CUDA_SUCCESS ? R9Q_OK : R9Q_ERR_LAUNCH;
 }
 
+int tmap_2d(const void* base, CUtensorMapDataType dt, int esize, int64_t rows, int64_t cols, int box_cols,
+            int box_rows, CUtensorMap* tm) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return R9Q_ERR_LAUNCH;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? R9Q_OK : R9Q_ERR_LAUNCH;
+}
+
+// Workspace of the tensor-core W8A8 path: [aq M x K][as M x KB fp32][ready m-tiles x int32]
+struct TcScratch {
+    size_t aq, as, ready, total;
+};
+TcScratch tc_scratch(int64_t M, int64_t K, bool need_aq) {
+    TcScratch t;
+    t.aq = 0;
+    t.as = need_aq ? align256((size_t)(M * K)) : 0;
+    t.ready = t.as + (need_aq ? align256((size_t)M * (K / 128) * 4) : 0);
+    t.total = t.ready + align256((size_t)((M + 127) / 128) * 4);
+    return t;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
@@ -111,8 +139,6 @@ int check_mnk(int64_t M, int64_t N, int64_t K) {
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? R9Q_OK : R9Q_ERR_LAUNCH; }
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 std::atomic<int> g_pdl{0};
 
@@ -355,7 +381,9 @@ int r9q_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t N2, int
         case R9Q_OP_GEMM_W8BF16: {
             int rc = check_mnk(M, N, K);
             if (rc) return rc;
-            *bytes = 0;      // split-K is reduced in distributed shared memory
+            // decode widths: split-K is reduced in distributed shared memory (no
+            // scratch); W8A8 above 64 rows quantises A once into scratch
+            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= kTcMinM) ? tc_scratch(M, K, true).total : 0;
             return R9Q_OK;
         }
         case R9Q_OP_GATE_UP_SWIGLU_DOWN: {
@@ -390,11 +418,39 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     if (a_bf16 && aq && (overlaps(aq, (size_t)(M * K), a_bf16, 2 * (size_t)(M * K)) ||
                          overlaps(aq, (size_t)(M * K), w, (size_t)(N * K))))
         return R9Q_ERR_ARG;
+    if (M >= kTcMinM) {
+        // tensor-core path: needs scratch for the ready counters, and for the
+        // quantised A unless the caller asked for aq/as as outputs
+        const bool need_aq = a_bf16 && !aq;
+        const TcScratch sc = tc_scratch(M, K, need_aq);
+        const size_t need = a_bf16 ? sc.total : 0;
+        if (need > 0 && (!workspace || workspace_bytes < need)) return R9Q_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return R9Q_ERR_ALIGN;
+        if (need > 0 && (overlaps(workspace, need, y_bf16, ybytes) || overlaps(workspace, need, a_bf16, 2 * (size_t)(M * K)) ||
+                         overlaps(workspace, need, w, (size_t)(N * K))))
+            return R9Q_ERR_ARG;
+    }
     DeviceInfo* d = nullptr;
     rc = current_device(&d);
     if (rc) return rc;
-    return run_stream_gemm(a_bf16 ? A_QUANT : A_PREQ, EPI_STORE, a_bf16, aq, as, w, ws, y_bf16, N, M, N, K, d,
-                           static_cast<cudaStream_t>(stream), g_pdl.load() != 0);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M < kTcMinM)
+        return run_stream_gemm(a_bf16 ? A_QUANT : A_PREQ, EPI_STORE, a_bf16, aq, as, w, ws, y_bf16, N, M, N, K, d, st,
+                               g_pdl.load() != 0);
+
+    const bool need_aq = a_bf16 && !aq;
+    const TcScratch sc = tc_scratch(M, K, need_aq);
+    uint8_t* wsp = static_cast<uint8_t*>(workspace);
+    uint8_t* aq_buf = need_aq ? wsp + sc.aq : aq;
+    float* as_buf = need_aq ? reinterpret_cast<float*>(wsp + sc.as) : as;
+    int* ready = a_bf16 ? reinterpret_cast<int*>(wsp + sc.ready) : nullptr;
+    CUtensorMap amap, bmap, ymap;
+    if ((rc = tmap_2d(aq_buf, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K, 128, 128, &amap)) != 0) return rc;
+    if ((rc = tmap_2d(w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K, 128, 256, &bmap)) != 0) return rc;
+    if ((rc = tmap_2d(y_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, 64, 128, &ymap)) != 0) return rc;
+    if (ready && cudaMemsetAsync(ready, 0, (size_t)((M + 127) / 128) * 4, st) != cudaSuccess) return R9Q_ERR_LAUNCH;
+    return to_status(launch_tc_gemm(amap, bmap, ymap, static_cast<const uint16_t*>(a_bf16), aq_buf, as_buf, ws, ready,
+                                    (int)M, (int)N, (int)K, d->err, d->sms, st));
 }
 
 int r9q_gemm_fp8w_bf16a(const void* a_bf16, const uint8_t* w, const float* ws, void* y_bf16, int64_t M,

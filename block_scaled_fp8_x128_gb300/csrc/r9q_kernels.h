@@ -61,6 +61,13 @@ cudaError_t launch_stream_a_bf16(const StreamPlan& plan, int epi, const CUtensor
 // is not touched again afterwards, so launches can be captured in graphs).
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
+// ---- tcgen05 prefill GEMM (W8A8, M > 64) ----
+constexpr int kTcMinM = 65;
+size_t tc_smem_bytes();
+cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
+                           const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
+                           int K, int* err, int sms, cudaStream_t st);
+
 // ---- elementwise / quantisation ----
 cudaError_t launch_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, cudaStream_t st, int sms);
 cudaError_t launch_quant_group128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,

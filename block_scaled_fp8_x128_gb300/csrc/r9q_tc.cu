@@ -1,0 +1,400 @@
+// Prefill-width block-scaled fp8 GEMM on the 5th-generation tensor cores
+// (tcgen05 + TMEM), sm_103a.  W8A8 only; used for M > 64.
+//
+// The contraction is dense here (r9700-stack v0.3.0 notes: fp8 GEMMs on the
+// tiled tensor-core kernel at prefill sizes, and the exact block-scaled fp8
+// variant), so it runs on tcgen05:
+//  * persistent CTAs (one per SM) walk 128x256 output tiles in m-major order;
+//  * warp 0 streams A (128x128 e4m3) and B (256x128 e4m3) k-blocks with 2-D
+//    TMA, 128-byte swizzle, into a 3-stage shared-memory ring;
+//  * warp 1 issues tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32; four per
+//    128-wide k-block) into one of two TMEM partial buffers (2 x 256 fp32
+//    columns) and commits the stage and the buffer to mbarriers;
+//  * warps 4..11 (two warpgroups, 128 columns each) tcgen05.ld every k-block's
+//    partial and promote it into register accumulators with
+//    as[m][kb] * ws[nb][kb] -- the fp32 block scales cannot enter the MMA, so
+//    they are applied per k-block exactly as the block-scaled definition reads,
+//    while the tensor cores fill the other buffer;
+//  * the finished tile goes out as bf16 through a swizzled shared-memory
+//    staging area and TMA stores.
+// Fused activation quant (a_bf16 given): warps 2..3 quantise each A row
+// exactly once, per 128-wide group, into a global scratch copy (aq/as) that
+// the A loads read: every tile quantises its 1/(N/256) share of its m-tile's
+// 128 rows and adds them to a per-m-tile ready counter; the A loads of an
+// m-tile wait (bounded) until all 128 rows are in.  The codes and scales are
+// those of the standalone quant kernel, bit for bit.
+// All waits are bounded: a timeout records R9Q_ERR_TIMEOUT, the kernel drains
+// what it issued, frees its TMEM and returns.
+#include "r9q_device.cuh"
+#include "r9q_kernels.h"
+
+namespace r9q {
+
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int kStages = 3;
+constexpr int kABytes = BM * BK;                 // 16 KB
+constexpr int kBBytes = BN * BK;                 // 32 KB
+constexpr int kTcStageBytes = kABytes + kBBytes; // 48 KB
+constexpr int kOutBytes = 2 * 2 * 128 * 128;     // 2 warpgroups x 2 boxes x (128 rows x 128 B)
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;                     // warps 4..11
+constexpr uint32_t kTmemCols = 512;
+
+struct Params {
+    const uint16_t* a;        // bf16 activations [M][K] (fused) or nullptr
+    uint8_t* aq;              // e4m3 scratch / input [M][K]
+    float* as;                // fp32 scales [M][KB]
+    const float* ws;          // [NB][KB]
+    int* ready;               // [m-tiles] quantised-row counters (fused), zeroed before launch
+    int M, N, K, KB, NB;
+    int mtiles, ntiles;
+    int* err;
+};
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    // K-major operand, 128-byte swizzle: 8-row x 128-byte atoms stacked every
+    // 1024 bytes (stride byte offset); the leading byte offset is unused.
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                     // SWIZZLE_128B
+    return d;
+}
+
+// kind::f8f6f4 instruction descriptor: D fp32, A and B e4m3, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// bounded wait for `need` quantised rows of m-tile mt
+__device__ __forceinline__ bool wait_rows(const int* ready, int need) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (ld_acquire(ready) >= need) return true;
+        __nanosleep(128);
+    }
+    return false;
+}
+
+}  // namespace tc
+
+using namespace tc;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                   const __grid_constant__ CUtensorMap ymap, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* ring = smem;                                        // kStages x 48 KB
+    uint8_t* outst = smem + kStages * kTcStageBytes;               // 64 KB output staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(outst + kOutBytes);
+    uint64_t* full = bars;                                       // [kStages]
+    uint64_t* empty = bars + kStages;                            // [kStages]
+    uint64_t* tfull = bars + 2 * kStages;                        // [2] partial ready in TMEM
+    uint64_t* tempty = bars + 2 * kStages + 2;                   // [2] partial consumed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    int* flags = reinterpret_cast<int*>(tmem_slot + 2);          // [0] error, [1] ring issued, [2] mma k-blocks
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int total = p.mtiles * p.ntiles;
+    const int KB = p.KB;
+    const bool fused = p.a != nullptr;
+    volatile int* vflags = flags;
+    auto fail = [&]() {
+        record_error(p.err, kErrTimeout);
+        atomicExch(&flags[0], 1);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 8);                            // one arrive per epilogue warp
+        }
+        flags[0] = flags[1] = flags[2] = 0;
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
+                const int mt = t / p.ntiles, nt = t % p.ntiles;
+                if (fused) {
+                    const int need = min(BM, p.M - mt * BM);
+                    if (!wait_rows(p.ready + mt, need)) {
+                        fail();
+                        break;
+                    }
+                    fence_proxy_async_global();     // the TMA reads what generic stores wrote
+                }
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int st = it % kStages;
+                    if (it >= kStages && !mbar_wait(&empty[st], ((uint32_t)(it / kStages) & 1u) ^ 1u)) {
+                        fail();
+                        break;
+                    }
+                    uint8_t* sa = ring + st * kTcStageBytes;
+                    mbar_expect_tx(&full[st], kTcStageBytes);
+                    tma_load_2d(sa, &amap, kb * BK, mt * BM, &full[st]);
+                    tma_load_2d(sa + kABytes, &bmap, kb * BK, nt * BN, &full[st]);
+                    flags[1] = it + 1;
+                }
+                if (*vflags) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int st = it % kStages;
+                    const int ab = it & 1;
+                    if (!mbar_wait(&full[st], (uint32_t)(it / kStages) & 1u)) {
+                        fail();
+                        break;
+                    }
+                    if (it >= 2 && !mbar_wait(&tempty[ab], ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
+                        fail();
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(ring + st * kTcStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    const uint32_t td = tmem_base + (uint32_t)(ab * BN);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_f8(td, sdesc_sw128(sa + k * 32), sdesc_sw128(sb + k * 32), k > 0 ? 1u : 0u);
+                    mma_commit(&empty[st]);      // stage free once these MMAs have read it
+                    mma_commit(&tfull[ab]);      // partial ready for the epilogue
+                    flags[2] = it + 1;
+                }
+                if (*vflags) break;
+            }
+        }
+    } else if (warp < kEpiWarp0) {
+        // ---------------- A quantisation (fused mode) ----------------
+        if (fused) {
+            const int qw = warp - 2;                              // 0 or 1
+            const int rpt = (BM + p.ntiles - 1) / p.ntiles;       // rows per tile share
+            for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
+                const int mt = t / p.ntiles, nt = t % p.ntiles;
+                const int rows_mt = min(BM, p.M - mt * BM);
+                const int r_lo = min(nt * rpt, rows_mt), r_hi = min((nt + 1) * rpt, rows_mt);
+                int done = 0;
+                for (int r = r_lo + qw; r < r_hi; r += 2) {
+                    const int64_t row = (int64_t)mt * BM + r;
+                    const uint16_t* src = p.a + row * p.K;
+                    uint8_t* dq = p.aq + row * p.K;
+                    for (int g = 0; g < KB; ++g) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(src + g * BK + 4 * lane);
+                        float s;
+                        const uint32_t codes =
+                            quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s);
+                        *reinterpret_cast<uint32_t*>(dq + g * BK + 4 * lane) = codes;
+                        if (lane == 0) p.as[row * KB + g] = s;
+                    }
+                    ++done;
+                }
+                __syncwarp();
+                if (lane == 0 && done > 0) {
+                    fence_proxy_async_global();
+                    red_release_add(p.ready + mt, done);
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: promotion + store ----------------
+        const int ew = warp - kEpiWarp0;          // 0..7
+        const int wg = ew >> 2;                   // column half
+        const int q = warp & 3;                   // TMEM lane quarter of this warp
+        const int rl = q * 32 + lane;             // row within the tile
+        uint8_t* stg = outst + wg * (2 * 128 * 128);
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const int mt = t / p.ntiles, nt = t % p.ntiles;
+            const int nb = nt * 2 + wg;
+            const int64_t row = (int64_t)mt * BM + rl;
+            const bool row_ok = row < p.M;
+            // the scales of this m-tile come from the quant warps (of any CTA):
+            // wait (bounded, acquire) until all its rows are in
+            if (fused && *vflags == 0 && !wait_rows(p.ready + mt, min(BM, p.M - mt * BM))) fail();
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            float as_next = (row_ok) ? p.as[row * KB] : 0.0f;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int ab = it & 1;
+                const float as_cur = as_next;
+                if (kb + 1 < KB) as_next = row_ok ? p.as[row * KB + kb + 1] : 0.0f;
+                const float wsv = (nb < p.NB) ? p.ws[(int64_t)nb * KB + kb] : 0.0f;
+                const float sc = as_cur * wsv;
+                if (*vflags == 0 && !mbar_wait(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float v[16];
+                    tmem_ld16(taddr + c * 16, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(v[i], sc, acc[c * 16 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[ab]);
+            }
+            // ---- bf16 out: swizzled staging (two 64-column boxes) + TMA store ----
+            if (ew % 4 == 0 && lane == 0) bulk_wait_read0();   // previous tile's store has read the staging
+            named_sync(1 + wg, 128);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint8_t* box = stg + h * (128 * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[h * 64 + c * 8 + 0], acc[h * 64 + c * 8 + 1]);
+                    o.y = pack_bf16x2(acc[h * 64 + c * 8 + 2], acc[h * 64 + c * 8 + 3]);
+                    o.z = pack_bf16x2(acc[h * 64 + c * 8 + 4], acc[h * 64 + c * 8 + 5]);
+                    o.w = pack_bf16x2(acc[h * 64 + c * 8 + 6], acc[h * 64 + c * 8 + 7]);
+                    *reinterpret_cast<uint4*>(box + rl * 128 + ((c ^ (rl & 7)) << 4)) = o;
+                }
+            }
+            fence_proxy_async_smem();
+            named_sync(1 + wg, 128);
+            if (ew % 4 == 0 && lane == 0) {
+                const int col = nt * BN + wg * 128;
+                if (col < p.N) {
+                    tma_store_2d(&ymap, col, mt * BM, stg);
+                    if (col + 64 < p.N) tma_store_2d(&ymap, col + 64, mt * BM, stg + 128 * 128);
+                }
+                bulk_commit();
+            }
+        }
+        if (ew % 4 == 0 && lane == 0) bulk_wait0();
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    if (flags[0] != 0 && tid == 0) {
+        // drain what was issued: ring copies, then the MMAs' last commits
+        const int issued = flags[1];
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+            (void)mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u);
+        const int mmas = flags[2];
+        for (int i = max(0, mmas - 2); i < mmas; ++i) (void)mbar_wait(&tfull[i & 1], (uint32_t)(i >> 1) & 1u);
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+}
+
+size_t tc_smem_bytes() { return 1024 + (size_t)kStages * kTcStageBytes + kOutBytes + 256; }
+
+cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
+                           const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
+                           int K, int* err, int sms, cudaStream_t st) {
+    Params p;
+    p.a = a;
+    p.aq = aq;
+    p.as = as;
+    p.ws = ws;
+    p.ready = ready;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.KB = K / BK;
+    p.NB = N / 128;
+    p.mtiles = (M + BM - 1) / BM;
+    p.ntiles = (N + BN - 1) / BN;
+    p.err = err;
+    const size_t smem = tc_smem_bytes();
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(tc_gemm_kernel), smem);
+    if (e != cudaSuccess) return e;
+    const int total = p.mtiles * p.ntiles;
+    const int grid = total < sms ? total : sms;
+    tc_gemm_kernel<<<grid, kThreads, smem, st>>>(amap, bmap, ymap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace r9q
