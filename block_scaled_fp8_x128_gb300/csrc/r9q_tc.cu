@@ -263,13 +263,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t row = (int64_t)mt * BM + r;
                     const uint16_t* src = p.a + row * p.K;
                     uint8_t* dq = p.aq + row * p.K;
-                    for (int g = 0; g < KB; ++g) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(src + g * BK + 4 * lane);
-                        float s;
-                        const uint32_t codes =
-                            quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s);
-                        *reinterpret_cast<uint32_t*>(dq + g * BK + 4 * lane) = codes;
-                        if (lane == 0) p.as[row * KB + g] = s;
+                    // 16 groups of the row in flight at once, then quantised
+                    constexpr int CH = 16;
+                    for (int g0 = 0; g0 < KB; g0 += CH) {
+                        uint2 v[CH];
+#pragma unroll
+                        for (int j = 0; j < CH; ++j)
+                            if (g0 + j < KB) v[j] = *reinterpret_cast<const uint2*>(src + (g0 + j) * BK + 4 * lane);
+#pragma unroll
+                        for (int j = 0; j < CH; ++j) {
+                            if (g0 + j >= KB) break;
+                            float s;
+                            const uint32_t codes = quant_group128_warp(bf16_lo(v[j].x), bf16_hi(v[j].x),
+                                                                       bf16_lo(v[j].y), bf16_hi(v[j].y), s);
+                            *reinterpret_cast<uint32_t*>(dq + (g0 + j) * BK + 4 * lane) = codes;
+                            if (lane == 0) p.as[row * KB + g0 + j] = s;
+                        }
                     }
                     ++done;
                 }
@@ -309,13 +318,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*vflags == 0 && !mbar_wait(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
+                // two TMEM loads in flight per wait
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float v[16];
+                for (int c = 0; c < 8; c += 2) {
+                    float v[16], w[16];
                     tmem_ld16(taddr + c * 16, v);
+                    tmem_ld16(taddr + (c + 1) * 16, w);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(v[i], sc, acc[c * 16 + i]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[(c + 1) * 16 + i] = fmaf(w[i], sc, acc[(c + 1) * 16 + i]);
                 }
                 tc_fence_before();
                 __syncwarp();
