@@ -383,7 +383,7 @@ int r9q_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t N2, int
             if (rc) return rc;
             // decode widths: split-K is reduced in distributed shared memory (no
             // scratch); W8A8 above 64 rows quantises A once into scratch
-            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= kTcMinM) ? tc_scratch(M, K, true).total : 0;
+            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= kTcMinM && K / 128 <= tc_max_kb()) ? tc_scratch(M, K, true).total : 0;
             return R9Q_OK;
         }
         case R9Q_OP_GATE_UP_SWIGLU_DOWN: {
@@ -418,7 +418,8 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     if (a_bf16 && aq && (overlaps(aq, (size_t)(M * K), a_bf16, 2 * (size_t)(M * K)) ||
                          overlaps(aq, (size_t)(M * K), w, (size_t)(N * K))))
         return R9Q_ERR_ARG;
-    if (M >= kTcMinM) {
+    const bool tc_path = M >= kTcMinM && K / 128 <= tc_max_kb();
+    if (tc_path) {
         // tensor-core path: needs scratch for the ready counters, and for the
         // quantised A unless the caller asked for aq/as as outputs
         const bool need_aq = a_bf16 && !aq;
@@ -434,7 +435,7 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     rc = current_device(&d);
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M < kTcMinM)
+    if (!tc_path)
         return run_stream_gemm(a_bf16 ? A_QUANT : A_PREQ, EPI_STORE, a_bf16, aq, as, w, ws, y_bf16, N, M, N, K, d, st,
                                g_pdl.load() != 0);
 

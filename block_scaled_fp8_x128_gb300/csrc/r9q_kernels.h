@@ -64,6 +64,7 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 // ---- tcgen05 prefill GEMM (W8A8, M > 64) ----
 constexpr int kTcMinM = 65;
 size_t tc_smem_bytes();
+int tc_max_kb();            // largest K/128 the tensor-core path takes
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
                            const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
                            int K, int* err, int sms, cudaStream_t st);

@@ -37,7 +37,10 @@ constexpr int kStages = 3;
 constexpr int kABytes = BM * BK;                 // 16 KB
 constexpr int kBBytes = BN * BK;                 // 32 KB
 constexpr int kTcStageBytes = kABytes + kBBytes; // 48 KB
-constexpr int kOutBytes = 2 * 2 * 128 * 128;     // 2 warpgroups x 2 boxes x (128 rows x 128 B)
+constexpr int kOutBytes = 2 * 128 * 128;         // 2 warpgroups x one box (128 rows x 128 B)
+constexpr int kMaxKB = 96;                       // K <= 12288 on this path (scale staging)
+constexpr int kAsBytes = BM * (kMaxKB + 1) * 4;  // activation scales of a tile, rows padded
+constexpr int kWsBytes = 2 * kMaxKB * 4;         // weight scales of a tile
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;                     // warps 4..11
 constexpr uint32_t kTmemCols = 512;
@@ -148,8 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* ring = smem;                                        // kStages x 48 KB
-    uint8_t* outst = smem + kStages * kTcStageBytes;               // 64 KB output staging
-    uint64_t* bars = reinterpret_cast<uint64_t*>(outst + kOutBytes);
+    uint8_t* outst = smem + kStages * kTcStageBytes;             // output staging
+    float* as_s = reinterpret_cast<float*>(outst + kOutBytes);   // [BM][KB + 1]
+    float* ws_s = as_s + BM * (kMaxKB + 1);                      // [2][KB]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ws_s + 2 * kMaxKB);
     uint64_t* full = bars;                                       // [kStages]
     uint64_t* empty = bars + kStages;                            // [kStages]
     uint64_t* tfull = bars + 2 * kStages;                        // [2] partial ready in TMEM
@@ -295,7 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = ew >> 2;                   // column half
         const int q = warp & 3;                   // TMEM lane quarter of this warp
         const int rl = q * 32 + lane;             // row within the tile
-        uint8_t* stg = outst + wg * (2 * 128 * 128);
+        const int wtid = ew * 32 + lane - wg * 128;   // 0..127 within the warpgroup
+        const bool leader = (ew & 3) == 0 && lane == 0;
+        uint8_t* stg = outst + wg * (128 * 128);
+        float* as_row = as_s + rl * (KB + 1);
+        float* ws_wg = ws_s + wg * KB;
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const int mt = t / p.ntiles, nt = t % p.ntiles;
@@ -305,16 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the scales of this m-tile come from the quant warps (of any CTA):
             // wait (bounded, acquire) until all its rows are in
             if (fused && *vflags == 0 && !wait_rows(p.ready + mt, min(BM, p.M - mt * BM))) fail();
+            // stage this tile's scales: my row's activation scales, my
+            // warpgroup's weight-block scales (all loads in flight together)
+            named_sync(1 + wg, 128);              // previous tile's readers are done
+            for (int kb = 0; kb < KB; ++kb) as_row[kb] = row_ok ? p.as[row * KB + kb] : 0.0f;
+            for (int kb = wtid; kb < KB; kb += 128) ws_wg[kb] = (nb < p.NB) ? p.ws[(int64_t)nb * KB + kb] : 0.0f;
+            named_sync(1 + wg, 128);
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-            float as_next = (row_ok) ? p.as[row * KB] : 0.0f;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int ab = it & 1;
-                const float as_cur = as_next;
-                if (kb + 1 < KB) as_next = row_ok ? p.as[row * KB + kb + 1] : 0.0f;
-                const float wsv = (nb < p.NB) ? p.ws[(int64_t)nb * KB + kb] : 0.0f;
-                const float sc = as_cur * wsv;
+                const float sc = as_row[kb] * ws_wg[kb];
                 if (*vflags == 0 && !mbar_wait(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
@@ -334,12 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[ab]);
             }
-            // ---- bf16 out: swizzled staging (two 64-column boxes) + TMA store ----
-            if (ew % 4 == 0 && lane == 0) bulk_wait_read0();   // previous tile's store has read the staging
-            named_sync(1 + wg, 128);
+            // ---- bf16 out: two 64-column boxes through the swizzled staging, TMA stores ----
+            const int col0 = nt * BN + wg * 128;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                uint8_t* box = stg + h * (128 * 128);
+                if (leader) bulk_wait_read0();    // the previous store has read the staging
+                named_sync(1 + wg, 128);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 o;
@@ -347,21 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o.y = pack_bf16x2(acc[h * 64 + c * 8 + 2], acc[h * 64 + c * 8 + 3]);
                     o.z = pack_bf16x2(acc[h * 64 + c * 8 + 4], acc[h * 64 + c * 8 + 5]);
                     o.w = pack_bf16x2(acc[h * 64 + c * 8 + 6], acc[h * 64 + c * 8 + 7]);
-                    *reinterpret_cast<uint4*>(box + rl * 128 + ((c ^ (rl & 7)) << 4)) = o;
+                    *reinterpret_cast<uint4*>(stg + rl * 128 + ((c ^ (rl & 7)) << 4)) = o;
                 }
-            }
-            fence_proxy_async_smem();
-            named_sync(1 + wg, 128);
-            if (ew % 4 == 0 && lane == 0) {
-                const int col = nt * BN + wg * 128;
-                if (col < p.N) {
-                    tma_store_2d(&ymap, col, mt * BM, stg);
-                    if (col + 64 < p.N) tma_store_2d(&ymap, col + 64, mt * BM, stg + 128 * 128);
+                fence_proxy_async_smem();
+                named_sync(1 + wg, 128);
+                if (leader) {
+                    if (col0 + 64 * h < p.N) tma_store_2d(&ymap, col0 + 64 * h, mt * BM, stg);
+                    bulk_commit();
                 }
-                bulk_commit();
             }
         }
-        if (ew % 4 == 0 && lane == 0) bulk_wait0();
+        if (leader) bulk_wait0();
     }
 
     // ---------------- teardown ----------------
@@ -382,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
 }
 
-size_t tc_smem_bytes() { return 1024 + (size_t)kStages * kTcStageBytes + kOutBytes + 256; }
+size_t tc_smem_bytes() { return 1024 + (size_t)kStages * kTcStageBytes + kOutBytes + kAsBytes + kWsBytes + 256; }
+int tc_max_kb() { return kMaxKB; }
 
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
                            const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
