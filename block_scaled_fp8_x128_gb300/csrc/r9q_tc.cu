@@ -17,12 +17,12 @@
 //    while the tensor cores fill the other buffer;
 //  * the finished tile goes out as bf16 through a swizzled shared-memory
 //    staging area and TMA stores.
-// Fused activation quant (a_bf16 given): warps 2..3 quantise each A row
-// exactly once, per 128-wide group, into a global scratch copy (aq/as) that
-// the A loads read: every tile quantises its 1/(N/256) share of its m-tile's
-// 128 rows and adds them to a per-m-tile ready counter; the A loads of an
-// m-tile wait (bounded) until all 128 rows are in.  The codes and scales are
-// those of the standalone quant kernel, bit for bit.
+// Fused activation quant (a_bf16 given): before taking up their roles, all
+// warps of the grid quantise each A row exactly once, per 128-wide group, into
+// a global scratch copy (aq/as) that the A loads read, dealing rows out in
+// global order and counting finished rows per m-tile; the A loads (and the
+// scale reads) of an m-tile wait (bounded) until its rows are all in.  The
+// codes and scales are those of the standalone quant kernel, bit for bit.
 // All waits are bounded: a timeout records R9Q_ERR_TIMEOUT, the kernel drains
 // what it issued, frees its TMEM and returns.
 #include "r9q_device.cuh"
@@ -195,6 +195,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    if (fused) {
+        // ---------------- quant phase: every warp of the grid ----------------
+        // Rows are dealt out in global order (warp w of the grid takes rows
+        // w, w + 12*grid, ...), so m-tiles fill up from the top while the
+        // GEMM roles below start on the first ones.  Each finished row is
+        // published to its m-tile's ready counter.
+        const int gw = blockIdx.x * (kThreads / 32) + warp;
+        const int GW = gridDim.x * (kThreads / 32);
+        for (int64_t row = gw; row < p.M; row += GW) {
+            const uint16_t* src = p.a + row * p.K;
+            uint8_t* dq = p.aq + row * p.K;
+            constexpr int CH = 8;                  // groups of the row in flight at once
+            for (int g0 = 0; g0 < KB; g0 += CH) {
+                uint2 v[CH];
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    if (g0 + j < KB) v[j] = *reinterpret_cast<const uint2*>(src + (g0 + j) * BK + 4 * lane);
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    if (g0 + j >= KB) break;
+                    float s;
+                    const uint32_t codes = quant_group128_warp(bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y),
+                                                               bf16_hi(v[j].y), s);
+                    *reinterpret_cast<uint32_t*>(dq + (g0 + j) * BK + 4 * lane) = codes;
+                    if (lane == 0) p.as[row * KB + g0 + j] = s;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_global();
+                red_release_add(p.ready + row / BM, 1);
+            }
+        }
+    }
+
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -255,45 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp < kEpiWarp0) {
-        // ---------------- A quantisation (fused mode) ----------------
-        if (fused) {
-            const int qw = warp - 2;                              // 0 or 1
-            const int rpt = (BM + p.ntiles - 1) / p.ntiles;       // rows per tile share
-            for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
-                const int mt = t / p.ntiles, nt = t % p.ntiles;
-                const int rows_mt = min(BM, p.M - mt * BM);
-                const int r_lo = min(nt * rpt, rows_mt), r_hi = min((nt + 1) * rpt, rows_mt);
-                int done = 0;
-                for (int r = r_lo + qw; r < r_hi; r += 2) {
-                    const int64_t row = (int64_t)mt * BM + r;
-                    const uint16_t* src = p.a + row * p.K;
-                    uint8_t* dq = p.aq + row * p.K;
-                    // 16 groups of the row in flight at once, then quantised
-                    constexpr int CH = 16;
-                    for (int g0 = 0; g0 < KB; g0 += CH) {
-                        uint2 v[CH];
-#pragma unroll
-                        for (int j = 0; j < CH; ++j)
-                            if (g0 + j < KB) v[j] = *reinterpret_cast<const uint2*>(src + (g0 + j) * BK + 4 * lane);
-#pragma unroll
-                        for (int j = 0; j < CH; ++j) {
-                            if (g0 + j >= KB) break;
-                            float s;
-                            const uint32_t codes = quant_group128_warp(bf16_lo(v[j].x), bf16_hi(v[j].x),
-                                                                       bf16_lo(v[j].y), bf16_hi(v[j].y), s);
-                            *reinterpret_cast<uint32_t*>(dq + (g0 + j) * BK + 4 * lane) = codes;
-                            if (lane == 0) p.as[row * KB + g0 + j] = s;
-                        }
-                    }
-                    ++done;
-                }
-                __syncwarp();
-                if (lane == 0 && done > 0) {
-                    fence_proxy_async_global();
-                    red_release_add(p.ready + mt, done);
-                }
-            }
-        }
+        // warps 2..3: no role after the quant phase
     } else {
         // ---------------- epilogue: promotion + store ----------------
         const int ew = warp - kEpiWarp0;          // 0..7
@@ -414,8 +411,19 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     if (e != cudaSuccess) return e;
     const int total = p.mtiles * p.ntiles;
     const int grid = total < sms ? total : sms;
-    tc_gemm_kernel<<<grid, kThreads, smem, st>>>(amap, bmap, ymap, p);
-    return cudaGetLastError();
+    // Every CTA quantises rows other CTAs wait for, so all CTAs must be
+    // resident at once: a cooperative launch guarantees it (one CTA per SM).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, amap, bmap, ymap, p);
 }
 
 }  // namespace r9q
