@@ -40,22 +40,39 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// q = e4m3(fl32(x / s)) without a division per element.  y = x * (1/s) with
-// the correctly rounded reciprocal is within 2 fp32 ulps of fl32(x/s); the
-// e4m3 rounding of a value only depends on which side of an e4m3 midpoint it
-// lies, and for |y| >= 2^-6 those midpoints are exactly the fp32 values whose
-// low 20 mantissa bits are 0x80000.  So y gives the same code unless it lies
-// within 2 ulps of such a midpoint or in the e4m3 subnormal range, and those
-// (rare) elements take the IEEE division.  `r` must be finite.
+// fl32(a / 448) without a division: y0 = a * RN(1/448), the residual
+// a - 448*y0 is exact in one FMA, and y0 + residual * RN(1/448) rounds to
+// the IEEE quotient.  Checked against IEEE division for every finite bf16 a
+// (the group maxima are bf16 values); tests/test_quant_arith.py.
+__device__ __forceinline__ float div448(float a) {
+    const float c = __uint_as_float(0x3B124925u);     // RN(1/448)
+    const float y0 = __fmul_rn(a, c);
+    const float r = __fmaf_rn(-448.0f, y0, a);
+    return __fmaf_rn(r, c, y0);
+}
+
+// q = e4m3(fl32(x / s)) without a division per element.  With r the hardware
+// reciprocal of s (relative error below 2^-22) y = x*r lies within 6 fp32
+// ulps of fl32(x/s).  The e4m3 rounding of a value only depends on which side
+// of an e4m3 midpoint it lies, and for |v| >= 2^-6 those midpoints are exactly
+// the fp32 values whose low 20 mantissa bits are 0x80000.  So y gives the same
+// code unless it lies within 8 ulps of such a midpoint or in the e4m3
+// subnormal range; those rare elements take the IEEE division.
 __device__ __forceinline__ float quot_for_e4m3(float x, float s, float r) {
     const float y = __fmul_rn(x, r);
     const uint32_t lo = __float_as_uint(y) & 0xFFFFFu;
-    if (fabsf(y) < 0x1p-6f || (lo - 0x7FFFEu) <= 4u) return __fdiv_rn(x, s);
+    if (fabsf(y) < 0x1p-6f || (lo - 0x7FFF8u) <= 16u) return __fdiv_rn(x, s);
     return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float s) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return r;
+}
+
 // Group-128 quantisation of one group held by a full warp: lane l holds
-// x[4l .. 4l+3].  scale = amax/448 (IEEE fp32 division); codes = e4m3(x/scale)
+// x[4l .. 4l+3].  scale = amax/448 (IEEE fp32 quotient); codes = e4m3(x/scale)
 // exactly as one IEEE fp32 division per element would give (see
 // quot_for_e4m3); amax == 0 gives scale 0, codes 0.  Returns the lane's 4
 // codes packed little-endian (x[4l] in bits 0..7).
@@ -64,12 +81,12 @@ __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, floa
     float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, 448.0f);
+    const float s = div448(amax);
     scale = s;
     if (amax == 0.0f) return 0u;
-    const float r = __frcp_rn(s);
+    const float r = rcp_approx(s);
     float t0, t1, t2, t3;
-    if (r < 0x1p127f) {            // finite reciprocal (s is not a tiny subnormal)
+    if (s >= 0x1p-125f) {          // reciprocal comfortably finite and normal
         t0 = quot_for_e4m3(v0, s, r);
         t1 = quot_for_e4m3(v1, s, r);
         t2 = quot_for_e4m3(v2, s, r);
@@ -81,6 +98,45 @@ __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, floa
         t3 = __fdiv_rn(v3, s);
     }
     return cvt_e4m3x2(t0, t1) | (cvt_e4m3x2(t2, t3) << 16);
+}
+
+// Four groups at once (independent chains interleaved for ILP): group j's
+// lane values are the bf16 pairs in v[j]; same results as quant_group128_warp.
+__device__ __forceinline__ void quant_group128_warp_x4(const uint2 (&v)[4], uint32_t (&codes)[4],
+                                                       float (&scale)[4]) {
+    float x[4][4], amax[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        x[j][0] = bf16_lo(v[j].x);
+        x[j][1] = bf16_hi(v[j].x);
+        x[j][2] = bf16_lo(v[j].y);
+        x[j][3] = bf16_hi(v[j].y);
+        amax[j] = fmaxf(fmaxf(fabsf(x[j][0]), fabsf(x[j][1])), fmaxf(fabsf(x[j][2]), fabsf(x[j][3])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+    float s[4], r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s[j] = div448(amax[j]);
+        r[j] = rcp_approx(s[j]);
+        scale[j] = s[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float t[4];
+        if (s[j] >= 0x1p-125f) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) t[e] = quot_for_e4m3(x[j][e], s[j], r[j]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) t[e] = __fdiv_rn(x[j][e], s[j]);
+        }
+        const uint32_t c = cvt_e4m3x2(t[0], t[1]) | (cvt_e4m3x2(t[2], t[3]) << 16);
+        codes[j] = (amax[j] == 0.0f) ? 0u : c;
+    }
 }
 
 // silu(g) * u in fp32 (g, u already bf16-rounded); the separate-launch SwiGLU

@@ -211,15 +211,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint2 v[CH];
 #pragma unroll
                 for (int j = 0; j < CH; ++j)
-                    if (g0 + j < KB) v[j] = *reinterpret_cast<const uint2*>(src + (g0 + j) * BK + 4 * lane);
+                    v[j] = (g0 + j < KB) ? *reinterpret_cast<const uint2*>(src + (g0 + j) * BK + 4 * lane)
+                                         : make_uint2(0u, 0u);
 #pragma unroll
-                for (int j = 0; j < CH; ++j) {
-                    if (g0 + j >= KB) break;
-                    float s;
-                    const uint32_t codes = quant_group128_warp(bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y),
-                                                               bf16_hi(v[j].y), s);
-                    *reinterpret_cast<uint32_t*>(dq + (g0 + j) * BK + 4 * lane) = codes;
-                    if (lane == 0) p.as[row * KB + g0 + j] = s;
+                for (int j0 = 0; j0 < CH; j0 += 4) {
+                    if (g0 + j0 >= KB) break;
+                    const uint2 w4[4] = {v[j0], v[j0 + 1], v[j0 + 2], v[j0 + 3]};
+                    uint32_t codes[4];
+                    float sc[4];
+                    quant_group128_warp_x4(w4, codes, sc);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (g0 + j0 + j >= KB) break;
+                        *reinterpret_cast<uint32_t*>(dq + (g0 + j0 + j) * BK + 4 * lane) = codes[j];
+                        if (lane == 0) p.as[row * KB + g0 + j0 + j] = sc[j];
+                    }
                 }
             }
             __syncwarp();

@@ -112,6 +112,27 @@ def test_quant_quotient_every_bf16_value(r9q):
     assert bad[0].size == 0, (bad[0][:5], bad[1][:5])
 
 
+def test_quant_every_bf16_group_max(r9q):
+    """One group per positive finite bf16 maximum (32,639 groups): scales and
+    codes bit-exact against the oracle's fp32 divisions."""
+    rng = np.random.default_rng(78)
+    amax = np.arange(1, 0x7F80, dtype=np.uint16)
+    af = f32_of_bits(amax).astype(np.float64)
+    frac = rng.uniform(-1.0, 1.0, (amax.size, 127))
+    xs = synth.to_bf16_bits((frac * af[:, None]).astype(np.float32))
+    xs_f = f32_of_bits(xs)
+    xs = np.where(np.abs(xs_f) <= af[:, None], xs, np.uint16(0))      # keep amax the group maximum
+    groups = np.concatenate([amax[:, None], xs], axis=1)
+    pad = (-groups.shape[0]) % 8
+    groups = np.concatenate([groups, np.zeros((pad, 128), np.uint16)])
+    xb = groups.reshape(-1, 1024)
+    xq, xsc = r9q.r9q_quant_group128(bf16_to_dev(xb))
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_group(xb)
+    assert np.array_equal(xsc.cpu().numpy(), os_)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+
+
 def test_weight_block_quant_bit_exact(r9q):
     quantised_weights(r9q, 0, 512, 1024)
     quantised_weights(r9q, 1, 4096, 4096)
