@@ -368,6 +368,32 @@ def run_reference(args):
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case(case, calls):
+    """A few plain calls of one workload, for ncu; prints nothing to time."""
+    import torch
+    import block_scaled_fp8_x128_gb300 as r9q
+    import synth
+    dev = torch.device("cuda", 0)
+    if case == "c3":
+        M, H, I, Ho = 8, 4096, 1536, 4096
+        x = torch.from_numpy(synth.to_bf16_bits(synth.activations(3, M, H)).view(np.int16)).view(torch.bfloat16).to(dev)
+        wgu, sgu = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(3, 2 * I, H, tensor=1)).to(dev))
+        wdn, sdn = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(3, Ho, I, tensor=2)).to(dev))
+        for _ in range(calls):
+            r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn)
+    else:
+        M, N, K, seed, wonly = {"c1": (16, 4096, 4096, 1, True), "c4-8192": (8192, 4096, 4096, 4, False),
+                                "c2-16": (16, 12288, 4096, 2, False)}[case]
+        copies = max(1, min(8, _copies_for(gemm_bytes(M, N, K))))
+        X, W, S, Y = _make_inputs(torch, r9q, "w8a8", M, N, K, seed, 0.0, 1.0, copies, dev)
+        for i in range(calls):
+            if wonly:
+                r9q.r9q_gemm_fp8w_bf16a(X[i % copies], W[i % copies], S[i % copies], y=Y[i % copies])
+            else:
+                r9q.r9q_gemm_fp8_block_qa(X[i % copies], W[i % copies], S[i % copies], y=Y[i % copies])
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -379,8 +405,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     ap.add_argument("--no-pdl", action="store_true", help="launch every GEMM fully serialised")
+    ap.add_argument("--profile-case", choices=["c1", "c4-8192", "c2-16", "c3"], default=None,
+                    help="only run a few calls of one workload (for an external profiler) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.profile_case:
+        profile_case(args.profile_case, args.steps)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
