@@ -25,6 +25,10 @@ NVCC_FLAGS = [
 ]
 
 
+# per-translation-unit extra nvcc flags
+PER_FILE_FLAGS: dict[str, list[str]] = {}
+
+
 def _nvcc():
     cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
     return cand if os.path.exists(cand) else "nvcc"
@@ -49,7 +53,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc, *NVCC_FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *NVCC_FLAGS, *PER_FILE_FLAGS.get(os.path.basename(src), []), "-c", src, "-o", obj]
             if verbose_ptxas:
                 cmd[1:1] = ["-Xptxas", "-v"]
             procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
