@@ -10,7 +10,7 @@
 //  * warp 1 issues tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32; four per
 //    128-wide k-block) into one of two TMEM partial buffers (2 x 256 fp32
 //    columns) and commits the stage and the buffer to mbarriers;
-//  * warps 2..9 (two warpgroups, 128 columns each) tcgen05.ld every k-block's
+//  * warps 4..11 (two warpgroups, 128 columns each) tcgen05.ld every k-block's
 //    partial and promote it into register accumulators with
 //    as[m][kb] * ws[nb][kb] -- the fp32 block scales cannot enter the MMA, so
 //    they are applied per k-block exactly as the block-scaled definition reads,
@@ -41,8 +41,8 @@ constexpr int kOutBytes = 2 * 128 * 128;         // 2 warpgroups x one box (128 
 constexpr int kMaxKB = 96;                       // K <= 12288 on this path (scale staging)
 constexpr int kAsBytes = BM * (kMaxKB + 1) * 4;  // activation scales of a tile, rows padded
 constexpr int kWsBytes = 2 * kMaxKB * 4;         // weight scales of a tile
-constexpr int kThreads = 320;                   // producer, MMA, 8 epilogue warps
-constexpr int kEpiWarp0 = 2;                     // warps 2..9
+constexpr int kThreads = 384;                   // producer, MMA, 2 spare, 8 epilogue warps
+constexpr int kEpiWarp0 = 4;                     // warps 4..11
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -90,26 +90,22 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 64 consecutive TMEM columns of this thread's lane, and the wait for them in
+// 32 consecutive TMEM columns of this thread's lane, and the wait for them in
 // the same asm statement, so no use of the registers can be scheduled before
 // the data has arrived.
-__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, float (&v)[64]) {
-    uint32_t r[64];
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, const void* src) {
@@ -151,8 +147,8 @@ __device__ __forceinline__ bool wait_rows(const int* ready, int need) {
 
 using namespace tc;
 
-// 320 threads x 200 registers = 64,000 of the SM's 65,536 (one CTA per SM)
-__global__ void __maxnreg__(200)
+// 12 warps: each SM sub-partition holds 3 of them, so up to 168 registers a thread
+__global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const __grid_constant__ CUtensorMap ymap, const Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -305,6 +301,8 @@ __global__ void __maxnreg__(200)
                 if (*vflags) break;
             }
         }
+    } else if (warp < kEpiWarp0) {
+        // warps 2..3: only the quant phase
     } else {
         // ---------------- epilogue: promotion + store ----------------
         const int ew = warp - kEpiWarp0;          // 0..7
@@ -341,11 +339,11 @@ __global__ void __maxnreg__(200)
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float v[64];
-                    tmem_ld64_wait(taddr + c * 64, v);
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_ld32_wait(taddr + c * 32, v);
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[c * 64 + i] = fmaf(v[i], sc, acc[c * 64 + i]);
+                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
                 }
                 tc_fence_before();
                 __syncwarp();
