@@ -100,8 +100,18 @@ __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, floa
     return cvt_e4m3x2(t0, t1) | (cvt_e4m3x2(t2, t3) << 16);
 }
 
+// true when y = x * (1/s) might not give the code of fl32(x / s): y within 8
+// ulps of an e4m3 rounding midpoint, or in the e4m3 subnormal range
+__device__ __forceinline__ bool quot_risky(float y) {
+    const uint32_t lo = __float_as_uint(y) & 0xFFFFFu;
+    return fabsf(y) < 0x1p-6f || (lo - 0x7FFF8u) <= 16u;
+}
+
 // Four groups at once (independent chains interleaved for ILP): group j's
 // lane values are the bf16 pairs in v[j]; same results as quant_group128_warp.
+// The common case is branch-free; only when some lane of the warp holds a
+// risky quotient (or a tiny scale) does the warp redo those elements with the
+// IEEE division.
 __device__ __forceinline__ void quant_group128_warp_x4(const uint2 (&v)[4], uint32_t (&codes)[4],
                                                        float (&scale)[4]) {
     float x[4][4], amax[4];
@@ -117,24 +127,31 @@ __device__ __forceinline__ void quant_group128_warp_x4(const uint2 (&v)[4], uint
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
-    float s[4], r[4];
+    float s[4], r[4], t[4][4];
+    bool risky = false;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         s[j] = div448(amax[j]);
         r[j] = rcp_approx(s[j]);
         scale[j] = s[j];
+        const bool live = amax[j] != 0.0f;
+        risky |= live && !(s[j] >= 0x1p-125f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            t[j][e] = __fmul_rn(x[j][e], r[j]);
+            risky |= live && quot_risky(t[j][e]);
+        }
+    }
+    if (__any_sync(0xffffffffu, risky)) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (amax[j] != 0.0f && (!(s[j] >= 0x1p-125f) || quot_risky(t[j][e]))) t[j][e] = __fdiv_rn(x[j][e], s[j]);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        float t[4];
-        if (s[j] >= 0x1p-125f) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) t[e] = quot_for_e4m3(x[j][e], s[j], r[j]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) t[e] = __fdiv_rn(x[j][e], s[j]);
-        }
-        const uint32_t c = cvt_e4m3x2(t[0], t[1]) | (cvt_e4m3x2(t[2], t[3]) << 16);
+        const uint32_t c = cvt_e4m3x2(t[j][0], t[j][1]) | (cvt_e4m3x2(t[j][2], t[j][3]) << 16);
         codes[j] = (amax[j] == 0.0f) ? 0u : c;
     }
 }
