@@ -39,6 +39,8 @@ _SIGS = {
                                  _P, _SZ, _P], ctypes.c_int),
     "r9q_workspace_bytes": ([ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(_SZ)],
                             ctypes.c_int),
+    "r9q_gate_up_swiglu_down_noalloc": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, ctypes.c_int, _P],
+                                        ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -221,4 +223,29 @@ def r9q_gate_up_swiglu_down(x: torch.Tensor, w_gu: torch.Tensor, s_gu: torch.Ten
     _check(_lib.r9q_gate_up_swiglu_down(_ptr(x), _ptr(w_gu), _ptr(s_gu), _ptr(w_dn), _ptr(s_dn), _ptr(y),
                                         M, H, I, H_out, _ptr(h), _ptr(hq), _ptr(hs), int(flags),
                                         _ptr(workspace), wsb, _stream(stream)), "r9q_gate_up_swiglu_down")
+    return y
+
+
+def r9q_gate_up_swiglu_down_noalloc(x: torch.Tensor, w_gu: torch.Tensor, s_gu: torch.Tensor, w_dn: torch.Tensor,
+                                    s_dn: torch.Tensor, y: torch.Tensor | None = None,
+                                    hq: torch.Tensor | None = None, hs: torch.Tensor | None = None,
+                                    flags: int = 0, stream=None) -> torch.Tensor:
+    """The fused expert MLP without workspace (h lives in the library's fixed
+    scratch; see include/r9q.h for the size limit and the sharing rules)."""
+    M, H = x.shape
+    I = w_gu.shape[0] // 2
+    H_out = w_dn.shape[0]
+    _expect(x, torch.bfloat16, (M, H), "x")
+    _expect(w_gu, torch.uint8, (2 * I, H), "w_gu")
+    _expect(s_gu, torch.float32, (2 * I // 128, H // 128), "s_gu")
+    _expect(w_dn, torch.uint8, (H_out, I), "w_dn")
+    _expect(s_dn, torch.float32, (H_out // 128, I // 128), "s_dn")
+    _expect(hq, torch.uint8, (M, I), "hq")
+    _expect(hs, torch.float32, (M, I // 128), "hs")
+    if y is None:
+        y = torch.empty((M, H_out), dtype=torch.bfloat16, device=x.device)
+    _expect(y, torch.bfloat16, (M, H_out), "y")
+    _check(_lib.r9q_gate_up_swiglu_down_noalloc(_ptr(x), _ptr(w_gu), _ptr(s_gu), _ptr(w_dn), _ptr(s_dn), _ptr(y),
+                                                M, H, I, H_out, _ptr(hq), _ptr(hs), int(flags), _stream(stream)),
+           "r9q_gate_up_swiglu_down_noalloc")
     return y

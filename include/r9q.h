@@ -152,6 +152,26 @@ int r9q_gate_up_swiglu_down(const void* x_bf16,
                             void* h_bf16_out, uint8_t* hq_out, float* hs_out, int flags,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of r9q_gate_up_swiglu_down, for callers that cannot
+ * allocate device memory where they run the MLP (an arena or pool owner that
+ * hands out no scratch, a plug-in that only receives its input and output
+ * buffers, code that must not call cudaMalloc).  The pages have no counterpart:
+ * this is a library convenience.  Same arguments and results as the fused path
+ * of r9q_gate_up_swiglu_down (flags may hold R9Q_MLP_WEIGHT_ONLY; R9Q_MLP_UNFUSED
+ * is rejected with R9Q_ERR_ARG) except that there is no h output and no
+ * workspace: h lives in a scratch array inside the library, 1 MiB per GPU held
+ * from load until process exit, so M * I must not exceed 524288 (larger sizes
+ * return R9Q_ERR_WORKSPACE).  The call allocates nothing.  The first call on a
+ * device looks up that device's scratch address (cudaGetSymbolAddress with the
+ * device current), so make that first call before capturing a stream.  All
+ * calls share the one scratch array, which is fully rewritten by each call:
+ * calls that can overlap on the GPU (different streams) race on it. */
+int r9q_gate_up_swiglu_down_noalloc(const void* x_bf16,
+                                    const uint8_t* w_gu, const float* s_gu,
+                                    const uint8_t* w_dn, const float* s_dn,
+                                    void* y_bf16, int64_t M, int64_t H, int64_t I, int64_t H_out,
+                                    uint8_t* hq_out, float* hs_out, int flags, void* stream);
+
 /* Workspace query. */
 #define R9Q_OP_GEMM_W8A8            1   /* (M, N, K) */
 #define R9Q_OP_GEMM_W8BF16          2   /* (M, N, K) */
