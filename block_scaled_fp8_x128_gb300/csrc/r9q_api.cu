@@ -8,6 +8,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -142,6 +143,18 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? R9Q_OK : R9Q_ERR_LAUNCH
 
 std::atomic<int> g_pdl{0};
 
+// Tuning override "S,G,stages" for tests and benches (R9Q_PLAN); 0 fields = planner's choice.
+void env_plan(int* S, int* G, int* st) {
+    static int v[3] = {-1, 0, 0};
+    if (v[0] < 0) {
+        v[0] = v[1] = v[2] = 0;
+        if (const char* s = std::getenv("R9Q_PLAN")) std::sscanf(s, "%d,%d,%d", &v[0], &v[1], &v[2]);
+    }
+    *S = v[0];
+    *G = v[1];
+    *st = v[2];
+}
+
 int env_splits() {
     static int v = -1;
     if (v < 0) {
@@ -230,6 +243,16 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
                     bst = st;
                     break;
                 }
+        }
+    }
+    {
+        int fS, fG, fst;
+        env_plan(&fS, &fG, &fst);
+        if (fS > 0 && fS <= maxS && KB % fS == 0 && fG > 0 && ntiles % fG == 0 && fst >= 2 && fst <= kMaxStages &&
+            stream_smem_bytes(MT, amode, KB / fS, ntiles / fG, fst) <= kSmemLimit) {
+            bS = fS;
+            bG = fG;
+            bst = fst;
         }
     }
     if (bS < 0) return false;
