@@ -217,6 +217,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Bounded wait that sleeps in hardware: each try_wait suspends the thread for up
+// to `hint_ns` unless the phase completes first, so a waiting warp takes no
+// issue slots from the warps that do the work.  False after `tries` attempts.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 20000,
+                                                uint32_t tries = 1u << 16) {
+    for (uint32_t i = 0; i < tries; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
 // Bounded wait for the phase with the given parity; false after kSpinLimit
 // tries.  try_wait itself suspends the thread for a while in hardware, so the
 // loop polls without sleeping (a software sleep would oversleep the arrival).

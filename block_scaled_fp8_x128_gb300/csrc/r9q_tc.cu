@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int st = it % kStages;
-                    if (it >= kStages && !mbar_wait(&empty[st], ((uint32_t)(it / kStages) & 1u) ^ 1u)) {
+                    if (it >= kStages && !mbar_wait_sleep(&empty[st], ((uint32_t)(it / kStages) & 1u) ^ 1u)) {
                         fail();
                         break;
                     }
@@ -279,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int st = it % kStages;
                     const int ab = it & 1;
-                    if (!mbar_wait(&full[st], (uint32_t)(it / kStages) & 1u)) {
+                    if (!mbar_wait_sleep(&full[st], (uint32_t)(it / kStages) & 1u)) {
                         fail();
                         break;
                     }
-                    if (it >= 2 && !mbar_wait(&tempty[ab], ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
+                    if (it >= 2 && !mbar_wait_sleep(&tempty[ab], ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
                         fail();
                         break;
                     }
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int ab = it & 1;
                 const float sc = as_row[kb] * ws_wg[kb];
-                if (*vflags == 0 && !mbar_wait(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
+                if (*vflags == 0 && !mbar_wait_sleep(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
 #pragma unroll
