@@ -326,7 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage this tile's scales: my row's activation scales, my
             // warpgroup's weight-block scales (all loads in flight together)
             named_sync(1 + wg, 128);              // previous tile's readers are done
-            for (int kb = 0; kb < KB; ++kb) as_row[kb] = row_ok ? p.as[row * KB + kb] : 0.0f;
+            // this row's KB scales, 16 loads in flight at a time
+            for (int k0 = 0; k0 < KB; k0 += 16) {
+                float tmp[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) tmp[j] = (row_ok && k0 + j < KB) ? p.as[row * KB + k0 + j] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (k0 + j < KB) as_row[k0 + j] = tmp[j];
+            }
             for (int kb = wtid; kb < KB; kb += 128) ws_wg[kb] = (nb < p.NB) ? p.ws[(int64_t)nb * KB + kb] : 0.0f;
             named_sync(1 + wg, 128);
             float acc[128];
