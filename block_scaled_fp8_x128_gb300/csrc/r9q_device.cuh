@@ -51,31 +51,30 @@ __device__ __forceinline__ float div448(float a) {
     return __fmaf_rn(r, c, y0);
 }
 
-// q = e4m3(fl32(x / s)) without a division per element.  With r the hardware
-// reciprocal of s (relative error below 2^-22) y = x*r lies within 6 fp32
-// ulps of fl32(x/s).  The e4m3 rounding of a value only depends on which side
-// of an e4m3 midpoint it lies, and for |v| >= 2^-6 those midpoints are exactly
-// the fp32 values whose low 20 mantissa bits are 0x80000.  So y gives the same
-// code unless it lies within 8 ulps of such a midpoint or in the e4m3
-// subnormal range; those rare elements take the IEEE division.
-__device__ __forceinline__ float quot_for_e4m3(float x, float s, float r) {
-    const float y = __fmul_rn(x, r);
-    const uint32_t lo = __float_as_uint(y) & 0xFFFFFu;
-    if (fabsf(y) < 0x1p-6f || (lo - 0x7FFF8u) <= 16u) return __fdiv_rn(x, s);
-    return y;
-}
+// fl32(x / s) without a division, for bf16 x and a scale s = fl32(amax/448)
+// of a bf16 amax: with r = RN(1/s), y = RN(x*r), e = RN(x - s*y) (one FMA)
+// and RN(y + e*r) (one FMA) is the IEEE quotient.  Rounding commutes with
+// scaling by powers of two, so only the significands of x and amax matter:
+// tests/test_quant_arith.py runs all 128 x 128 pairs in exact arithmetic.
+// The reduction to significands needs no underflow in e, which holds for
+// s >= 2^-90 whenever |x/s| >= 2^-11 (the lowest bit of s*y is at least
+// 2^-147); smaller quotients give the e4m3 code 0 either way.  Callers send
+// groups with smaller scales through the IEEE division.  The residual is
+// formed as s*y - x and subtracted, so that x = -0 gives -0 (x - s*y would
+// give +0 and the code 0x00 instead of 0x80).
+constexpr float kQuotExactMinScale = 0x1p-90f;
 
-__device__ __forceinline__ float rcp_approx(float s) {
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
-    return r;
+__device__ __forceinline__ float quot_exact(float x, float s, float r) {
+    const float y = __fmul_rn(x, r);
+    const float e = __fmaf_rn(s, y, -x);
+    return __fmaf_rn(-e, r, y);
 }
 
 // Group-128 quantisation of one group held by a full warp: lane l holds
 // x[4l .. 4l+3].  scale = amax/448 (IEEE fp32 quotient); codes = e4m3(x/scale)
-// exactly as one IEEE fp32 division per element would give (see
-// quot_for_e4m3); amax == 0 gives scale 0, codes 0.  Returns the lane's 4
-// codes packed little-endian (x[4l] in bits 0..7).
+// with x/scale the IEEE fp32 quotient (see quot_exact); amax == 0 gives scale
+// 0, codes 0.  Returns the lane's 4 codes packed little-endian (x[4l] in bits
+// 0..7).
 __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, float v2, float v3,
                                                         float& scale) {
     float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
@@ -84,13 +83,13 @@ __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, floa
     const float s = div448(amax);
     scale = s;
     if (amax == 0.0f) return 0u;
-    const float r = rcp_approx(s);
     float t0, t1, t2, t3;
-    if (s >= 0x1p-125f) {          // reciprocal comfortably finite and normal
-        t0 = quot_for_e4m3(v0, s, r);
-        t1 = quot_for_e4m3(v1, s, r);
-        t2 = quot_for_e4m3(v2, s, r);
-        t3 = quot_for_e4m3(v3, s, r);
+    if (s >= kQuotExactMinScale) {
+        const float r = __frcp_rn(s);
+        t0 = quot_exact(v0, s, r);
+        t1 = quot_exact(v1, s, r);
+        t2 = quot_exact(v2, s, r);
+        t3 = quot_exact(v3, s, r);
     } else {
         t0 = __fdiv_rn(v0, s);
         t1 = __fdiv_rn(v1, s);
@@ -100,60 +99,46 @@ __device__ __forceinline__ uint32_t quant_group128_warp(float v0, float v1, floa
     return cvt_e4m3x2(t0, t1) | (cvt_e4m3x2(t2, t3) << 16);
 }
 
-// true when y = x * (1/s) might not give the code of fl32(x / s): y within 8
-// ulps of an e4m3 rounding midpoint, or in the e4m3 subnormal range
-__device__ __forceinline__ bool quot_risky(float y) {
-    const uint32_t lo = __float_as_uint(y) & 0xFFFFFu;
-    return fabsf(y) < 0x1p-6f || (lo - 0x7FFF8u) <= 16u;
-}
-
-// Four groups at once (independent chains interleaved for ILP): group j's
-// lane values are the bf16 pairs in v[j]; same results as quant_group128_warp.
-// The common case is branch-free; only when some lane of the warp holds a
-// risky quotient (or a tiny scale) does the warp redo those elements with the
-// IEEE division.
-__device__ __forceinline__ void quant_group128_warp_x4(const uint2 (&v)[4], uint32_t (&codes)[4],
-                                                       float (&scale)[4]) {
-    float x[4][4], amax[4];
+// Four groups per warp, eight lanes per group: lane l quantises values
+// x[16*(l&7) .. 16*(l&7)+15] of group l>>3, given as 16 bf16 in v[0], v[1].
+// Same results as quant_group128_warp, with three shuffle levels instead of
+// five and sixteen independent quotients per lane.  Returns the lane's 16
+// codes (x[16*(l&7)] in the low byte of .x).
+__device__ __forceinline__ uint4 quant_group128_lane8(const uint4 (&v)[2], float& scale) {
+    float x[16];
+    const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        x[j][0] = bf16_lo(v[j].x);
-        x[j][1] = bf16_hi(v[j].x);
-        x[j][2] = bf16_lo(v[j].y);
-        x[j][3] = bf16_hi(v[j].y);
-        amax[j] = fmaxf(fmaxf(fabsf(x[j][0]), fabsf(x[j][1])), fmaxf(fabsf(x[j][2]), fabsf(x[j][3])));
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w[i]);
+        x[2 * i + 1] = bf16_hi(w[i]);
     }
+    float a0 = fmaxf(fabsf(x[0]), fabsf(x[1])), a1 = fmaxf(fabsf(x[2]), fabsf(x[3]));
+    float a2 = fmaxf(fabsf(x[4]), fabsf(x[5])), a3 = fmaxf(fabsf(x[6]), fabsf(x[7]));
+    float a4 = fmaxf(fabsf(x[8]), fabsf(x[9])), a5 = fmaxf(fabsf(x[10]), fabsf(x[11]));
+    float a6 = fmaxf(fabsf(x[12]), fabsf(x[13])), a7 = fmaxf(fabsf(x[14]), fabsf(x[15]));
+    float amax = fmaxf(fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)), fmaxf(fmaxf(a4, a5), fmaxf(a6, a7)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float s = div448(amax);
+    scale = s;
+    const bool live = amax != 0.0f;
+    float t[16];
+    if (__any_sync(0xffffffffu, live && !(s >= kQuotExactMinScale))) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
+        for (int i = 0; i < 16; ++i) t[i] = __fdiv_rn(x[i], s);
+    } else {
+        const float r = __frcp_rn(s);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
-    float s[4], r[4], t[4][4];
-    bool risky = false;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        s[j] = div448(amax[j]);
-        r[j] = rcp_approx(s[j]);
-        scale[j] = s[j];
-        const bool live = amax[j] != 0.0f;
-        risky |= live && !(s[j] >= 0x1p-125f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            t[j][e] = __fmul_rn(x[j][e], r[j]);
-            risky |= live && quot_risky(t[j][e]);
-        }
+        for (int i = 0; i < 16; ++i) t[i] = quot_exact(x[i], s, r);
     }
-    if (__any_sync(0xffffffffu, risky)) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (amax[j] != 0.0f && (!(s[j] >= 0x1p-125f) || quot_risky(t[j][e]))) t[j][e] = __fdiv_rn(x[j][e], s[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t c = cvt_e4m3x2(t[j][0], t[j][1]) | (cvt_e4m3x2(t[j][2], t[j][3]) << 16);
-        codes[j] = (amax[j] == 0.0f) ? 0u : c;
-    }
+    uint4 c;
+    c.x = cvt_e4m3x2(t[0], t[1]) | (cvt_e4m3x2(t[2], t[3]) << 16);
+    c.y = cvt_e4m3x2(t[4], t[5]) | (cvt_e4m3x2(t[6], t[7]) << 16);
+    c.z = cvt_e4m3x2(t[8], t[9]) | (cvt_e4m3x2(t[10], t[11]) << 16);
+    c.w = cvt_e4m3x2(t[12], t[13]) | (cvt_e4m3x2(t[14], t[15]) << 16);
+    if (!live) c = make_uint4(0u, 0u, 0u, 0u);
+    return c;
 }
 
 // silu(g) * u in fp32 (g, u already bf16-rounded); the separate-launch SwiGLU

@@ -210,26 +210,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t row = gw; row < p.M; row += GW) {
             const uint16_t* src = p.a + row * p.K;
             uint8_t* dq = p.aq + row * p.K;
-            constexpr int CH = 32;                 // groups of the row in flight at once
+            // four groups per step (eight lanes each, 16 values a lane); the
+            // whole chunk of up to 32 groups is loaded before any is quantised
+            constexpr int CH = 32;
+            const int gl = lane >> 3, el = (lane & 7) * 16;
             for (int g0 = 0; g0 < KB; g0 += CH) {
-                uint2 v[CH];
+                uint4 v[CH / 4][2];
 #pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    v[j] = (g0 + j < KB) ? *reinterpret_cast<const uint2*>(src + (g0 + j) * BK + 4 * lane)
-                                         : make_uint2(0u, 0u);
+                for (int j = 0; j < CH / 4; ++j) {
+                    const int g = g0 + 4 * j + gl;
+                    if (g < KB) {
+                        const uint4* q = reinterpret_cast<const uint4*>(src + (int64_t)g * BK + el);
+                        v[j][0] = q[0];
+                        v[j][1] = q[1];
+                    } else {
+                        v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
 #pragma unroll
-                for (int j0 = 0; j0 < CH; j0 += 4) {
-                    if (g0 + j0 < KB) {
-                        const uint2 w4[4] = {v[j0], v[j0 + 1], v[j0 + 2], v[j0 + 3]};
-                        uint32_t codes[4];
-                        float sc[4];
-                        quant_group128_warp_x4(w4, codes, sc);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (g0 + j0 + j < KB) {
-                                *reinterpret_cast<uint32_t*>(dq + (g0 + j0 + j) * BK + 4 * lane) = codes[j];
-                                if (lane == 0) p.as[row * KB + g0 + j0 + j] = sc[j];
-                            }
+                for (int j = 0; j < CH / 4; ++j) {
+                    if (g0 + 4 * j < KB) {
+                        const int g = g0 + 4 * j + gl;
+                        float sc;
+                        const uint4 codes = quant_group128_lane8(v[j], sc);
+                        if (g < KB) {
+                            *reinterpret_cast<uint4*>(dq + (int64_t)g * BK + el) = codes;
+                            if ((lane & 7) == 0) p.as[row * KB + g] = sc;
                         }
                     }
                 }

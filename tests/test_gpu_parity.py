@@ -82,11 +82,11 @@ def test_quant_group128_bit_exact(r9q, M, K, p, factor, seed):
     assert np.array_equal(xq.cpu().numpy(), oq)
 
 
-def test_quant_quotient_every_bf16_value(r9q):
-    """The quantiser's division-free quotient against the oracle's fp32 division:
-    every finite bf16 magnitude x, both signs, against 600 group maxima (random
-    bf16 values plus subnormal, tiny and huge ones), as groups [amax, x...]."""
-    rng = np.random.default_rng(77)
+def _every_value_groups(seed=77):
+    """Groups [amax, x...]: every finite bf16 magnitude x, both signs, against
+    600 group maxima (random bf16 values plus subnormal, tiny and huge ones);
+    rows of K = 1024."""
+    rng = np.random.default_rng(seed)
     all_pos = np.arange(0, 0x7F80, dtype=np.uint16)                    # finite non-negative bf16
     amaxes = np.concatenate([rng.integers(0x0001, 0x7F80, 590).astype(np.uint16),
                              np.uint16([0x0001, 0x0040, 0x0080, 0x0100, 0x0C00, 0x3F80, 0x43E0, 0x7F7F,
@@ -103,12 +103,36 @@ def test_quant_quotient_every_bf16_value(r9q):
         groups.append(np.concatenate([np.full((cand.shape[0], 1), a, np.uint16), cand], axis=1))
     flat = np.concatenate(groups)
     flat = np.concatenate([flat, np.zeros(((-flat.shape[0]) % 8, 128), np.uint16)])
-    xb = flat.reshape(-1, 1024)
+    return flat.reshape(-1, 1024)
+
+
+def test_quant_quotient_every_bf16_value(r9q):
+    """The quantiser's division-free quotient against the oracle's fp32 division."""
+    xb = _every_value_groups()
     xq, xs = r9q.r9q_quant_group128(bf16_to_dev(xb))
     torch.cuda.synchronize()
     oq, os_ = oracle.quant_group(xb)
     assert np.array_equal(xs.cpu().numpy(), os_)
     bad = np.nonzero(xq.cpu().numpy() != oq)
+    assert bad[0].size == 0, (bad[0][:5], bad[1][:5])
+
+
+@pytest.mark.parametrize("rows", [48, None])        # 48: decode kernel's A-load quant; all: prefill kernel
+def test_fused_quant_every_bf16_value(r9q, rows):
+    """The GEMMs' fused activation quant (decode A-load and the prefill
+    kernel's quant phase) on the same groups: codes and scales bit-exact."""
+    xb = _every_value_groups()
+    if rows is not None:
+        xb = xb[:rows]
+    M, K = xb.shape
+    wq, ws = quantised_weights(r9q, 5, 256, K, check_oracle=False)
+    aq = torch.empty((M, K), dtype=torch.uint8, device=dev())
+    a_s = torch.empty((M, K // 128), dtype=torch.float32, device=dev())
+    r9q.r9q_gemm_fp8_block_qa(bf16_to_dev(xb), wq, ws, aq=aq, as_=a_s)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_group(xb)
+    assert np.array_equal(a_s.cpu().numpy(), os_)
+    bad = np.nonzero(aq.cpu().numpy() != oq)
     assert bad[0].size == 0, (bad[0][:5], bad[1][:5])
 
 

@@ -48,3 +48,42 @@ def test_rn32_helper_agrees_with_numpy():
     x = rng.standard_normal(2000) * np.exp(rng.uniform(-60, 60, 2000))
     for v in x.tolist():
         assert np.float32(float(_rn32(Fraction(v)))) == np.float32(v)
+
+
+
+def test_fma_corrected_quotient_is_ieee_for_bf16():
+    """The quantisers compute x/s as r = RN(1/s), y = RN(x*r),
+    e = RN(x - s*y) (FMA), q = RN(y + e*r) (FMA), with s = fl32(amax/448).
+    For bf16 x and amax, q must be the IEEE quotient fl32(x/s).  Every
+    rounding commutes with scaling by powers of two (no underflow, which the
+    kernels guarantee by their scale guard), so the significands of x and
+    amax decide: all 128 x 128 pairs, each step in exact arithmetic with one
+    rounding, x above and below amax's significand."""
+    bad = []
+    for am in range(128):
+        amax = Fraction(128 + am, 128)
+        s = _rn32(amax / 448)
+        r = _rn32(1 / s)
+        for xm in range(128):
+            for xe in (0, -1):
+                x = Fraction(128 + xm, 128) * Fraction(2) ** xe
+                y = _rn32(x * r)
+                e = _rn32(x - s * y)
+                q = _rn32(y + e * r)
+                if q != _rn32(x / s):
+                    bad.append((am, xm, xe))
+    assert not bad, bad[:5]
+
+
+def test_fma_corrected_quotient_needs_the_correction():
+    """The plain product RN(x * RN(1/s)) is not always the IEEE quotient for
+    these inputs, so the correction step is doing work (a dropped FMA would
+    fail the exhaustive test above)."""
+    miss = 0
+    for am in range(0, 128, 3):
+        s = _rn32(Fraction(128 + am, 128) / 448)
+        r = _rn32(1 / s)
+        for xm in range(128):
+            x = Fraction(128 + xm, 128)
+            miss += _rn32(x * r) != _rn32(x / s)
+    assert miss > 0
