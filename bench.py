@@ -56,6 +56,48 @@ def mlp_bytes(M, H, I, Ho):
     return gemm_bytes(M, 2 * I, H) - 2 * M * 2 * I + 2 * M * I + gemm_bytes(M, Ho, I) - 2 * M * I + 2 * M * I
 
 
+# ------------------------------------------------ captured DRAM traffic --
+
+# The sources each timed kernel is built from; a capture under profiles/ only
+# describes the kernel while these files are unchanged.
+KERNEL_SOURCES = {
+    "stream_gemm_kernel": ["r9q_api.cu", "r9q_device.cuh", "r9q_kernels.h", "r9q_stream.cuh", "r9q_stream_bf16.cu"],
+    "tc_gemm_kernel": ["r9q_api.cu", "r9q_device.cuh", "r9q_kernels.h", "r9q_tc.cu"],
+}
+
+
+def sources_hash(kernel):
+    import hashlib
+    d = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        rel = "block_scaled_fp8_x128_gb300/csrc/" + f
+        d.update(rel.encode())
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            d.update(fh.read())
+    return d.hexdigest()[:16]
+
+
+def captured_traffic(profile, kernel):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch from the ncu
+    summary profiles/<profile>, or None when the summary is missing or the
+    kernel's sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- `") and "`: " in line:
+                k, v = line[3:].split("`: ", 1)
+                kv[k.strip()] = v.strip().strip("`")
+    if kv.get("sources_sha256") != sources_hash(kernel):
+        return None
+    try:
+        return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
+    except (KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------- NVML clocks --
 
 class ClockSampler:
@@ -239,7 +281,8 @@ def run_gpu(args):
                    "timing": "CUDA-graph replay of exactly K calls, CUDA events on the replay stream",
                    "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gbs / hbm, 4), "traffic": None,
+                     "frac": round(gbs / hbm, 4),
+                     "traffic": captured_traffic("stream_gemm_w8bf16_M16_N4096_K4096.md", "stream_gemm_kernel"),
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback"},
         "e2e": {"value": None if args.no_e2e else round(bpc / (us_e2e * 1e-6) / 1e9, 1), "unit": "GB/s",
                 "us_per_call": None if args.no_e2e else round(us_e2e, 3),
