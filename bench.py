@@ -184,6 +184,11 @@ def _graph(torch, fn, n_calls, copies, stream):
     return g
 
 
+# Set by main() under torchrun: a barrier across ranks on both sides of every
+# timed region.
+_BARRIER = None
+
+
 def _time_steps(torch, fn, K, copies, stream, sampler=None):
     """Replay graphs covering exactly K calls; returns (ms_total)."""
     G = copies * max(1, 64 // copies)
@@ -199,6 +204,8 @@ def _time_steps(torch, fn, K, copies, stream, sampler=None):
         sampler.start()
     with torch.cuda.stream(stream):
         torch.cuda.synchronize()
+        if _BARRIER:
+            _BARRIER()
         e0.record(stream)
         for _ in range(reps):
             g_full.replay()
@@ -206,6 +213,8 @@ def _time_steps(torch, fn, K, copies, stream, sampler=None):
             g_rem.replay()
         e1.record(stream)
         torch.cuda.synchronize()
+        if _BARRIER:
+            _BARRIER()
     clocks = sampler.stop() if sampler else None
     return e0.elapsed_time(e1), clocks
 
@@ -213,7 +222,8 @@ def _time_steps(torch, fn, K, copies, stream, sampler=None):
 def run_gpu(args):
     import torch
     import block_scaled_fp8_x128_gb300 as r9q
-    dev = torch.device("cuda", 0)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     hbm, bf16, src = peaks()
     fp8_peak = 2.0 * bf16           # nominal fp8:bf16 dense ratio of 2 on the measured bf16 peak
@@ -236,7 +246,7 @@ def run_gpu(args):
         for i in range(args.warmup):
             step(i % copies)
     torch.cuda.synchronize()
-    sampler = ClockSampler(0)
+    sampler = ClockSampler(local)
     ms, clocks = _time_steps(torch, step, args.steps, copies, stream, sampler)
     us_call = ms * 1e3 / args.steps
     gbs = bpc / (us_call * 1e-6) / 1e9
@@ -303,7 +313,7 @@ def run_gpu(args):
 
 def sweep(torch, r9q, stream, hbm, fp8_peak, src):
     res = []
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
 
     def timeit(fn, copies, calls):
         with torch.cuda.stream(stream):
@@ -437,6 +447,32 @@ def profile_case(case, calls):
     torch.cuda.synchronize()
 
 
+def aggregate_over_ranks(out, world, all_reduce_max):
+    """Whole-job figures from one rank's result line.  Every rank runs the same
+    single-GPU step on its own GPU (replicas); all_reduce_max(x) returns the
+    maximum of x over the ranks.  value = the bytes all ranks moved per step
+    divided by the slowest rank's time per step."""
+    out = json.loads(json.dumps(out))
+    bpc = out["config"]["bytes_per_call"]
+    ms = all_reduce_max(out["ms_per_step"])
+    gbs_one = bpc / (ms * 1e-3) / 1e9
+    out["ms_per_step"] = ms
+    out["us_per_call"] = round(ms * 1e3, 3)
+    out["n_gpus"] = world
+    out["value"] = round(world * gbs_one, 1)
+    # the roofline stays per GPU: the dominant kernel at the slowest rank's pace
+    out["roofline"]["achieved"] = round(gbs_one, 1)
+    out["roofline"]["frac"] = round(gbs_one / out["roofline"]["peak"], 4)
+    e2e = out.get("e2e") or {}
+    us = e2e.get("us_per_call")
+    us = all_reduce_max(us if us is not None else -1.0)
+    if us > 0:
+        e2e["us_per_call"] = round(us, 3)
+        e2e["value"] = round(world * bpc / (us * 1e-6) / 1e9, 1)
+    out["gpu_launches"] = world * out["gpu_launches"]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,17 +502,24 @@ def main():
         # runs the same single-GPU step and rank 0 reports the aggregate
         import torch
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        global _BARRIER
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+        _BARRIER = dist.barrier
+        # the CPU baseline is timed on rank 0 alone
+        if rank != 0:
+            args.no_cpu_baseline = True
     out = run_gpu(args)
     if world > 1:
         import torch
         import torch.distributed as dist
-        t = torch.tensor([out["ms_per_step"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        out["ms_per_step"] = t.item()
-        out["n_gpus"] = world
-        out["value"] = round(out["value"] * world, 1)
+
+        def all_reduce_max(v):
+            t = torch.tensor([float(v)], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return t.item()
+        out = aggregate_over_ranks(out, world, all_reduce_max)
+        dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out))
 

@@ -236,6 +236,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// 2-D tiled TMA prefetch of box {c0 (inner), c1} into L2: no shared memory, no
+// completion to wait for; a later load of the same box then hits L2.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // 2-D tiled TMA load of box {c0 (inner), c1} into shared memory, completing on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1,
                                             uint64_t* bar) {

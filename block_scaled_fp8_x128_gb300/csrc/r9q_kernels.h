@@ -62,7 +62,7 @@ cudaError_t launch_stream_a_bf16(const StreamPlan& plan, int epi, const CUtensor
 cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
 // ---- tcgen05 prefill GEMM (W8A8, M > 64) ----
-constexpr int kTcMinM = 65;
+constexpr int kTcMinM = 33;
 size_t tc_smem_bytes();
 int tc_max_kb();            // largest K/128 the tensor-core path takes
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,

@@ -169,6 +169,15 @@ __global__ void __launch_bounds__(kStreamThreads)
             tma_load_2d(ring + it * kStageBytes + kStageBytes / 2, &wmap, (kb0 + i) * kBlock, r1, &full[it]);
         }
         flags[1] = npro;
+        // the rest of this CTA's weight slice goes to L2 now, so that the ring
+        // refills from L2 and the DRAM stream does not wait for the MMAs
+        for (int it = npro; it < iters; ++it) {
+            const int tl = it / nkb, i = it - tl * nkb;
+            int r0, r1, nb0, nb1;
+            tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
+            tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, r0);
+            tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, r1);
+        }
     }
     // Weights never come from the preceding kernel; activations and scales may.
     pdl_trigger();

@@ -261,7 +261,8 @@ def test_w8bf16_every_code_exact(r9q):
 # ----------------------------------------------------------- expert MLP --
 
 @pytest.mark.parametrize("weight_only", [False, True])
-@pytest.mark.parametrize("M,H,I,Ho", [(8, 4096, 1536, 4096), (3, 256, 384, 640), (20, 512, 256, 384)])
+@pytest.mark.parametrize("M,H,I,Ho", [(8, 4096, 1536, 4096), (3, 256, 384, 640), (20, 512, 256, 384),
+                                      (48, 512, 256, 384)])
 def test_mlp_fused_vs_unfused_and_oracle(r9q, weight_only, M, H, I, Ho):
     seed = 3
     xb = activations_bf16(seed, M, H)
