@@ -245,6 +245,13 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int c0, int
                  : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
+// It only fills L2, so it never returns stale data: data another kernel writes
+// afterwards replaces the lines in L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled TMA load of box {c0 (inner), c1} into shared memory, completing on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1,
                                             uint64_t* bar) {

@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(kStreamThreads)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
+    // The next kernel in the stream may start launching at once: it waits for
+    // this grid's completion itself before it reads anything this grid writes.
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.splits, G = p.groups, nst = p.stages;
     const int split = (int)cluster_ctarank();
@@ -179,8 +182,24 @@ __global__ void __launch_bounds__(kStreamThreads)
             tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, r1);
         }
     }
-    // Weights never come from the preceding kernel; activations and scales may.
-    pdl_trigger();
+    // Weights and their block scales never come from the preceding kernel:
+    // load the scales now.  The activation rows may: prefetch them into L2
+    // only (no stale data can result) and copy them after the wait.
+    if (producer) {
+        for (int tok = 0; tok < mvalid; ++tok) {
+            const uint8_t* src = (AMODE == A_PREQ)
+                ? p.aq + (int64_t)(m0 + tok) * p.K + (int64_t)kb0 * kBlock
+                : reinterpret_cast<const uint8_t*>(p.a + (int64_t)(m0 + tok) * p.K + (int64_t)kb0 * kBlock);
+            bulk_prefetch_l2(src, (uint32_t)row_bytes);
+        }
+    }
+    for (int c = tid; c < ntl * nkb; c += kStreamThreads) {
+        const int tl = c / nkb, i = c - tl * nkb;
+        int r0, r1, nb0, nb1;
+        tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
+        ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)nb0 * KB + kb0 + i];
+        ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)nb1 * KB + kb0 + i];
+    }
     pdl_wait();
     if (producer) {
         mbar_expect_tx(abar, (uint32_t)(mvalid * row_bytes));
@@ -192,13 +211,6 @@ __global__ void __launch_bounds__(kStreamThreads)
         }
     }
 
-    for (int c = tid; c < ntl * nkb; c += kStreamThreads) {
-        const int tl = c / nkb, i = c - tl * nkb;
-        int r0, r1, nb0, nb1;
-        tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
-        ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)nb0 * KB + kb0 + i];
-        ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)nb1 * KB + kb0 + i];
-    }
     // rows past the last token: zero codes / activations and zero scales
     for (int c = tid; c < (MT - mvalid) * (row_bytes / 16); c += kStreamThreads) {
         const int tok = mvalid + c / (row_bytes / 16), ch = c % (row_bytes / 16);
@@ -260,155 +272,164 @@ __global__ void __launch_bounds__(kStreamThreads)
             record_error(p.err, kErrTimeout);
             atomicExch(&flags[0], 1);
         };
-        for (int tl = 0; tl < ntl; ++tl) {
-            const int tile = group + tl * G;
-            float acc[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-            const float* wsv_s = ws_s + (tl * 2 + box) * kbs_max;
-            for (int i = 0; i < nkb; ++i) {
-                const int it = tl * nkb + i;
-                const int st = it % nst;
-                if (*vflags == 0 && !mbar_wait(&full[st], (uint32_t)(it / nst) & 1u)) fail();
-                const uint32_t tbase = smem_u32(ring + st * kStageBytes);
-                float d[NT][4];
+        // Tile tl's partial is parked and announced, then tile tl-1 is reduced:
+        // the wait for the peers' partials of one tile overlaps the MMAs of the next.
+        for (int tl = 0; tl <= ntl; ++tl) {
+            if (tl < ntl) {
+                float acc[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) d[nt][e] = 0.0f;
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+                const float* wsv_s = ws_s + (tl * 2 + box) * kbs_max;
+                for (int i = 0; i < nkb; ++i) {
+                    const int it = tl * nkb + i;
+                    const int st = it % nst;
+                    if (*vflags == 0 && !mbar_wait(&full[st], (uint32_t)(it / nst) & 1u)) fail();
+                    const uint32_t tbase = smem_u32(ring + st * kStageBytes);
+                    float d[NT][4];
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    uint32_t a[4];
-                    const int chunk = ks * 2 + lchk;
-                    ldmatrix_x4(tbase + row * 128 + ((chunk ^ (row & 7)) << 4), a[0], a[1], a[2], a[3]);
-                    if (AMODE != A_BF16) {
+                    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint8_t* bp = act + (nt * 8 + g) * act_ld + i * kBlock + ks * 32 + 4 * t;
-                            mma_e4m3_16832(d[nt], a, *reinterpret_cast<const uint32_t*>(bp),
-                                           *reinterpret_cast<const uint32_t*>(bp + 16));
-                        }
-                    } else {
-                        uint32_t ev[4], od[4];
+                        for (int e = 0; e < 4; ++e) d[nt][e] = 0.0f;
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) e4m3x4_to_bf16x2x2(a[r], ev[r], od[r]);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        uint32_t a[4];
+                        const int chunk = ks * 2 + lchk;
+                        ldmatrix_x4(tbase + row * 128 + ((chunk ^ (row & 7)) << 4), a[0], a[1], a[2], a[3]);
+                        if (AMODE != A_BF16) {
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint8_t* bp = act + (nt * 8 + g) * act_ld + 2 * (i * kBlock + ks * 32 + 4 * t);
-                            // (x0,x1),(x2,x3) -> (x0,x2),(x1,x3): the pairing of e4m3x4_to_bf16x2x2
-                            const uint2 bv = *reinterpret_cast<const uint2*>(bp);
-                            const uint2 cv = *reinterpret_cast<const uint2*>(bp + 32);
-                            mma_bf16_16816(d[nt], ev[0], ev[1], od[0], od[1], __byte_perm(bv.x, bv.y, 0x5410),
-                                           __byte_perm(bv.x, bv.y, 0x7632));
-                            mma_bf16_16816(d[nt], ev[2], ev[3], od[2], od[3], __byte_perm(cv.x, cv.y, 0x5410),
-                                           __byte_perm(cv.x, cv.y, 0x7632));
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint8_t* bp = act + (nt * 8 + g) * act_ld + i * kBlock + ks * 32 + 4 * t;
+                                mma_e4m3_16832(d[nt], a, *reinterpret_cast<const uint32_t*>(bp),
+                                               *reinterpret_cast<const uint32_t*>(bp + 16));
+                            }
+                        } else {
+                            uint32_t ev[4], od[4];
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) e4m3x4_to_bf16x2x2(a[r], ev[r], od[r]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const uint8_t* bp = act + (nt * 8 + g) * act_ld + 2 * (i * kBlock + ks * 32 + 4 * t);
+                                // (x0,x1),(x2,x3) -> (x0,x2),(x1,x3): the pairing of e4m3x4_to_bf16x2x2
+                                const uint2 bv = *reinterpret_cast<const uint2*>(bp);
+                                const uint2 cv = *reinterpret_cast<const uint2*>(bp + 32);
+                                mma_bf16_16816(d[nt], ev[0], ev[1], od[0], od[1], __byte_perm(bv.x, bv.y, 0x5410),
+                                               __byte_perm(bv.x, bv.y, 0x7632));
+                                mma_bf16_16816(d[nt], ev[2], ev[3], od[2], od[3], __byte_perm(cv.x, cv.y, 0x5410),
+                                               __byte_perm(cv.x, cv.y, 0x7632));
+                            }
                         }
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
+                    // block-scale promotion of this k-block's partial
+                    const float wsv = wsv_s[i];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float sc0 = wsv, sc1 = wsv;
+                        if (AMODE != A_BF16) {
+                            sc0 = as_s[(nt * 8 + 2 * t) * kbs_max + i] * wsv;
+                            sc1 = as_s[(nt * 8 + 2 * t + 1) * kbs_max + i] * wsv;
+                        }
+                        acc[nt][0] = fmaf(d[nt][0], sc0, acc[nt][0]);
+                        acc[nt][1] = fmaf(d[nt][1], sc1, acc[nt][1]);
+                        acc[nt][2] = fmaf(d[nt][2], sc0, acc[nt][2]);
+                        acc[nt][3] = fmaf(d[nt][3], sc1, acc[nt][3]);
+                    }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[st]);
-                // block-scale promotion of this k-block's partial
-                const float wsv = wsv_s[i];
+
+                // ---- park the partial in buffer b = tl & 1 (after its last readers are done) ----
+                const int b = tl & 1;
+                const uint32_t use = (uint32_t)(tl >> 1);
+                if (tl >= 2 && *vflags == 0 && !mbar_wait_cluster(&pfree[b], (use - 1) & 1u)) fail();
+                float* Pb = P + b * MT * kPStride;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float sc0 = wsv, sc1 = wsv;
-                    if (AMODE != A_BF16) {
-                        sc0 = as_s[(nt * 8 + 2 * t) * kbs_max + i] * wsv;
-                        sc1 = as_s[(nt * 8 + 2 * t + 1) * kbs_max + i] * wsv;
+                    const int r = warp * 16 + g;
+                    const int tok = nt * 8 + 2 * t;
+                    Pb[tok * kPStride + r] = acc[nt][0];
+                    Pb[(tok + 1) * kPStride + r] = acc[nt][1];
+                    Pb[tok * kPStride + r + 8] = acc[nt][2];
+                    Pb[(tok + 1) * kPStride + r + 8] = acc[nt][3];
+                }
+                consumer_sync();
+                if (tid == 0) mbar_arrive_all_ranks(&pfull[b], S);
+            }
+            if (tl >= 1) {
+                const int rt = tl - 1;
+                const int tile = group + rt * G;
+                const int b = rt & 1;
+                const uint32_t use = (uint32_t)(rt >> 1);
+                if (*vflags == 0 && !mbar_wait_cluster(&pfull[b], use & 1u)) fail();
+                const float* Pb = P + b * MT * kPStride;
+                // ---- split-K reduction of tile rt, slice `split`, over ranks 0..S-1 + epilogue ----
+                // Sums go to registers first; the peers are told their partials are
+                // free before the global stores, so the release never waits on them.
+                const uint32_t pbase = smem_u32(Pb);
+                constexpr int UPT = (EPI == EPI_SWIGLU) ? 32 : 64;   // units per token
+                constexpr int MAXU = (MT * UPT + kCWarps * 32 - 1) / (kCWarps * 32);   // units per thread, S = 1
+                const int U = MT * UPT;
+                const int u_lo = (split * U) / S, u_hi = ((split + 1) * U) / S;
+                uint32_t outv[MAXU];
+#pragma unroll
+                for (int j = 0; j < MAXU; ++j) {
+                    const int u = u_lo + tid + j * kCWarps * 32;
+                    outv[j] = 0u;
+                    if (u >= u_hi) continue;
+                    const int tok = u / UPT, up = u - tok * UPT;
+                    if (tok >= mvalid) continue;
+                    // all ranks' partials are loaded first (independent remote
+                    // loads in flight together), then summed in rank order
+                    if (EPI == EPI_STORE) {
+                        const uint32_t off = (uint32_t)((tok * kPStride + 2 * up) * 4);
+                        float2 v[kMaxSplits];
+#pragma unroll
+                        for (int r = 0; r < kMaxSplits; ++r)
+                            if (r < S) v[r] = ld_dsmem_f32x2(dsmem_addr(pbase + off, (uint32_t)r));
+                        float2 sum = v[0];
+#pragma unroll
+                        for (int r = 1; r < kMaxSplits; ++r)
+                            if (r < S) {
+                                sum.x = __fadd_rn(sum.x, v[r].x);
+                                sum.y = __fadd_rn(sum.y, v[r].y);
+                            }
+                        outv[j] = pack_bf16x2(sum.x, sum.y);
+                    } else {
+                        const uint32_t offg = (uint32_t)((tok * kPStride + 2 * up) * 4);
+                        const uint32_t offu = offg + 64 * 4;
+                        float2 gv[kMaxSplits], uv[kMaxSplits];
+#pragma unroll
+                        for (int r = 0; r < kMaxSplits; ++r)
+                            if (r < S) {
+                                gv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offg, (uint32_t)r));
+                                uv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offu, (uint32_t)r));
+                            }
+                        float2 gs = gv[0], us = uv[0];
+#pragma unroll
+                        for (int r = 1; r < kMaxSplits; ++r)
+                            if (r < S) {
+                                gs.x = __fadd_rn(gs.x, gv[r].x);
+                                gs.y = __fadd_rn(gs.y, gv[r].y);
+                                us.x = __fadd_rn(us.x, uv[r].x);
+                                us.y = __fadd_rn(us.y, uv[r].y);
+                            }
+                        const float h0 = silu_mul(bf16_round(gs.x), bf16_round(us.x));
+                        const float h1 = silu_mul(bf16_round(gs.y), bf16_round(us.y));
+                        outv[j] = pack_bf16x2(h0, h1);
                     }
-                    acc[nt][0] = fmaf(d[nt][0], sc0, acc[nt][0]);
-                    acc[nt][1] = fmaf(d[nt][1], sc1, acc[nt][1]);
-                    acc[nt][2] = fmaf(d[nt][2], sc0, acc[nt][2]);
-                    acc[nt][3] = fmaf(d[nt][3], sc1, acc[nt][3]);
                 }
-            }
-
-            // ---- park the partial in buffer b = tl & 1 (after its last readers are done) ----
-            const int b = tl & 1;
-            const uint32_t use = (uint32_t)(tl >> 1);
-            if (tl >= 2 && *vflags == 0 && !mbar_wait_cluster(&pfree[b], (use - 1) & 1u)) fail();
-            float* Pb = P + b * MT * kPStride;
+                consumer_sync();
+                if (tid == 0) mbar_arrive_all_ranks(&pfree[b], S);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int r = warp * 16 + g;
-                const int tok = nt * 8 + 2 * t;
-                Pb[tok * kPStride + r] = acc[nt][0];
-                Pb[(tok + 1) * kPStride + r] = acc[nt][1];
-                Pb[tok * kPStride + r + 8] = acc[nt][2];
-                Pb[(tok + 1) * kPStride + r + 8] = acc[nt][3];
-            }
-            consumer_sync();
-            if (tid == 0) mbar_arrive_all_ranks(&pfull[b], S);
-            if (*vflags == 0 && !mbar_wait_cluster(&pfull[b], use & 1u)) fail();
-
-            // ---- split-K reduction of slice `split` over ranks 0..S-1 + epilogue ----
-            // Sums go to registers first; the peers are told their partials are
-            // free before the global stores, so the release never waits on them.
-            const uint32_t pbase = smem_u32(Pb);
-            constexpr int UPT = (EPI == EPI_SWIGLU) ? 32 : 64;   // units per token
-            constexpr int MAXU = (MT * UPT + kCWarps * 32 - 1) / (kCWarps * 32);   // units per thread, S = 1
-            const int U = MT * UPT;
-            const int u_lo = (split * U) / S, u_hi = ((split + 1) * U) / S;
-            uint32_t outv[MAXU];
-#pragma unroll
-            for (int j = 0; j < MAXU; ++j) {
-                const int u = u_lo + tid + j * kCWarps * 32;
-                outv[j] = 0u;
-                if (u >= u_hi) continue;
-                const int tok = u / UPT, up = u - tok * UPT;
-                if (tok >= mvalid) continue;
-                // all ranks' partials are loaded first (independent remote
-                // loads in flight together), then summed in rank order
-                if (EPI == EPI_STORE) {
-                    const uint32_t off = (uint32_t)((tok * kPStride + 2 * up) * 4);
-                    float2 v[kMaxSplits];
-#pragma unroll
-                    for (int r = 0; r < kMaxSplits; ++r)
-                        if (r < S) v[r] = ld_dsmem_f32x2(dsmem_addr(pbase + off, (uint32_t)r));
-                    float2 sum = v[0];
-#pragma unroll
-                    for (int r = 1; r < kMaxSplits; ++r)
-                        if (r < S) {
-                            sum.x = __fadd_rn(sum.x, v[r].x);
-                            sum.y = __fadd_rn(sum.y, v[r].y);
-                        }
-                    outv[j] = pack_bf16x2(sum.x, sum.y);
-                } else {
-                    const uint32_t offg = (uint32_t)((tok * kPStride + 2 * up) * 4);
-                    const uint32_t offu = offg + 64 * 4;
-                    float2 gv[kMaxSplits], uv[kMaxSplits];
-#pragma unroll
-                    for (int r = 0; r < kMaxSplits; ++r)
-                        if (r < S) {
-                            gv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offg, (uint32_t)r));
-                            uv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offu, (uint32_t)r));
-                        }
-                    float2 gs = gv[0], us = uv[0];
-#pragma unroll
-                    for (int r = 1; r < kMaxSplits; ++r)
-                        if (r < S) {
-                            gs.x = __fadd_rn(gs.x, gv[r].x);
-                            gs.y = __fadd_rn(gs.y, gv[r].y);
-                            us.x = __fadd_rn(us.x, uv[r].x);
-                            us.y = __fadd_rn(us.y, uv[r].y);
-                        }
-                    const float h0 = silu_mul(bf16_round(gs.x), bf16_round(us.x));
-                    const float h1 = silu_mul(bf16_round(gs.y), bf16_round(us.y));
-                    outv[j] = pack_bf16x2(h0, h1);
+                for (int j = 0; j < MAXU; ++j) {
+                    const int u = u_lo + tid + j * kCWarps * 32;
+                    if (u >= u_hi) continue;
+                    const int tok = u / UPT, up = u - tok * UPT;
+                    if (tok >= mvalid) continue;
+                    const int64_t col = (EPI == EPI_STORE) ? (int64_t)kBlock * tile + 2 * up : (int64_t)64 * tile + 2 * up;
+                    *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + col) = outv[j];
                 }
-            }
-            consumer_sync();
-            if (tid == 0) mbar_arrive_all_ranks(&pfree[b], S);
-#pragma unroll
-            for (int j = 0; j < MAXU; ++j) {
-                const int u = u_lo + tid + j * kCWarps * 32;
-                if (u >= u_hi) continue;
-                const int tok = u / UPT, up = u - tok * UPT;
-                if (tok >= mvalid) continue;
-                const int64_t col = (EPI == EPI_STORE) ? (int64_t)kBlock * tile + 2 * up : (int64_t)64 * tile + 2 * up;
-                *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + col) = outv[j];
             }
         }
         // Peers stop touching this CTA's shared memory once every rank has
