@@ -43,6 +43,13 @@ constexpr int kAsBytes = BM * (kMaxKB + 1) * 4;  // activation scales of a tile,
 constexpr int kWsBytes = 2 * kMaxKB * 4;         // weight scales of a tile
 constexpr int kThreads = 384;                   // producer, MMA, 2 spare, 8 epilogue warps
 constexpr int kEpiWarp0 = 4;                     // warps 4..11
+// Registers a thread: at launch, and after the quant phase for warpgroup 0
+// (producer, MMA, two spare warps) and the two epilogue warpgroups.  The split
+// must add up to what the block was launched with, else setmaxnreg.inc would
+// wait for registers that never come free; the launcher checks the launch
+// count against the compiled kernel.
+constexpr int kLaunchRegs = 168, kRegsWg0 = 56, kRegsEpi = 224;
+static_assert(kRegsWg0 * 128 + kRegsEpi * 256 == kLaunchRegs * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -210,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t row = gw; row < p.M; row += GW) {
             const uint16_t* src = p.a + row * p.K;
             uint8_t* dq = p.aq + row * p.K;
+            // this warp's next row goes to L2 while this one is quantised
+            if (lane == 0 && row + GW < p.M) bulk_prefetch_l2(src + (int64_t)GW * p.K, (uint32_t)(2 * p.K));
             // four groups per step (eight lanes each, 16 values a lane); the
             // whole chunk of up to 32 groups is loaded before any is quantised
             constexpr int CH = 32;
@@ -248,68 +257,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            int it = 0;
-            for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
-                const int mt = t / p.ntiles, nt = t % p.ntiles;
-                if (fused) {
-                    const int need = min(BM, p.M - mt * BM);
-                    if (!wait_rows(p.ready + mt, need)) {
-                        fail();
-                        break;
+    // Registers move from warpgroup 0 (short loops) to the epilogue warpgroups
+    // (128 fp32 accumulators a thread).  Every warp gets to its setmaxnreg:
+    // the quant phase above has no waits.
+    if (warp < kEpiWarp0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+        if (warp == 0) {
+            // ---------------- TMA producer ----------------
+            if (lane == 0) {
+                int it = 0;
+                for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
+                    const int mt = t / p.ntiles, nt = t % p.ntiles;
+                    if (fused) {
+                        const int need = min(BM, p.M - mt * BM);
+                        if (!wait_rows(p.ready + mt, need)) {
+                            fail();
+                            break;
+                        }
+                        fence_proxy_async_global();     // the TMA reads what generic stores wrote
                     }
-                    fence_proxy_async_global();     // the TMA reads what generic stores wrote
-                }
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int st = it % kStages;
-                    if (it >= kStages && !mbar_wait_sleep(&empty[st], ((uint32_t)(it / kStages) & 1u) ^ 1u)) {
-                        fail();
-                        break;
+                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                        const int st = it % kStages;
+                        if (it >= kStages && !mbar_wait_sleep(&empty[st], ((uint32_t)(it / kStages) & 1u) ^ 1u)) {
+                            fail();
+                            break;
+                        }
+                        uint8_t* sa = ring + st * kTcStageBytes;
+                        mbar_expect_tx(&full[st], kTcStageBytes);
+                        tma_load_2d(sa, &amap, kb * BK, mt * BM, &full[st]);
+                        tma_load_2d(sa + kABytes, &bmap, kb * BK, nt * BN, &full[st]);
+                        flags[1] = it + 1;
                     }
-                    uint8_t* sa = ring + st * kTcStageBytes;
-                    mbar_expect_tx(&full[st], kTcStageBytes);
-                    tma_load_2d(sa, &amap, kb * BK, mt * BM, &full[st]);
-                    tma_load_2d(sa + kABytes, &bmap, kb * BK, nt * BN, &full[st]);
-                    flags[1] = it + 1;
+                    if (*vflags) break;
                 }
-                if (*vflags) break;
             }
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            int it = 0;
-            for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int st = it % kStages;
-                    const int ab = it & 1;
-                    if (!mbar_wait_sleep(&full[st], (uint32_t)(it / kStages) & 1u)) {
-                        fail();
-                        break;
-                    }
-                    if (it >= 2 && !mbar_wait_sleep(&tempty[ab], ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
-                        fail();
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(ring + st * kTcStageBytes);
-                    const uint32_t sb = sa + kABytes;
-                    const uint32_t td = tmem_base + (uint32_t)(ab * BN);
+        } else if (warp == 1) {
+            // ---------------- MMA issuer ----------------
+            if (lane == 0) {
+                int it = 0;
+                for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
+                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                        const int st = it % kStages;
+                        const int ab = it & 1;
+                        if (!mbar_wait_sleep(&full[st], (uint32_t)(it / kStages) & 1u)) {
+                            fail();
+                            break;
+                        }
+                        if (it >= 2 && !mbar_wait_sleep(&tempty[ab], ((uint32_t)(it >> 1) & 1u) ^ 1u)) {
+                            fail();
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(ring + st * kTcStageBytes);
+                        const uint32_t sb = sa + kABytes;
+                        const uint32_t td = tmem_base + (uint32_t)(ab * BN);
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        mma_f8(td, sdesc_sw128(sa + k * 32), sdesc_sw128(sb + k * 32), k > 0 ? 1u : 0u);
-                    mma_commit(&empty[st]);      // stage free once these MMAs have read it
-                    mma_commit(&tfull[ab]);      // partial ready for the epilogue
-                    flags[2] = it + 1;
+                        for (int k = 0; k < BK / 32; ++k)
+                            mma_f8(td, sdesc_sw128(sa + k * 32), sdesc_sw128(sb + k * 32), k > 0 ? 1u : 0u);
+                        mma_commit(&empty[st]);      // stage free once these MMAs have read it
+                        mma_commit(&tfull[ab]);      // partial ready for the epilogue
+                        flags[2] = it + 1;
+                    }
+                    if (*vflags) break;
                 }
-                if (*vflags) break;
             }
         }
-    } else if (warp < kEpiWarp0) {
         // warps 2..3: only the quant phase
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         // ---------------- epilogue: promotion + store ----------------
         const int ew = warp - kEpiWarp0;          // 0..7
         const int wg = ew >> 2;                   // column half
@@ -356,12 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) {
                     float v[32];
                     tmem_ld32_wait(taddr + c * 32, v);
+                    if (c == 3) {
+                        // the whole partial is in registers: free the buffer
+                        // for the MMA two k-blocks ahead before the last FMAs
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[ab]);
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[ab]);
             }
             // ---- bf16 out: two 64-column boxes through the swizzled staging, TMA stores ----
             const int col0 = nt * BN + wg * 128;
@@ -428,6 +447,12 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     p.ntiles = (N + BN - 1) / BN;
     p.err = err;
     const size_t smem = tc_smem_bytes();
+    // The kernel's register split assumes the compiled launch count.
+    static const int launch_regs = []() {
+        cudaFuncAttributes fa = {};
+        return cudaFuncGetAttributes(&fa, tc_gemm_kernel) == cudaSuccess ? fa.numRegs : -1;
+    }();
+    if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(tc_gemm_kernel), smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
