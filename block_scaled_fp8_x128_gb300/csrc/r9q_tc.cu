@@ -39,8 +39,12 @@ constexpr int kBBytes = BN * BK;                 // 32 KB
 constexpr int kTcStageBytes = kABytes + kBBytes; // 48 KB
 constexpr int kOutBytes = 2 * 128 * 128;         // 2 warpgroups x one box (128 rows x 128 B)
 constexpr int kMaxKB = 96;                       // K <= 12288 on this path (scale staging)
-constexpr int kAsBytes = BM * (kMaxKB + 1) * 4;  // activation scales of a tile, rows padded
+constexpr int kAsBytes = BM * (kMaxKB + 1) * 4;  // activation scales of a tile: [KB][BM + 1] fp32
 constexpr int kWsBytes = 2 * kMaxKB * 4;         // weight scales of a tile
+// With KB <= 48 the scale areas hold two tiles, so the staging warps fill the
+// next tile's scales while the epilogue works on the current one.
+constexpr int kAsDoubleMaxKB = (BM * (kMaxKB + 1)) / (2 * (BM + 1));
+static_assert(kMaxKB * (BM + 1) <= BM * (kMaxKB + 1), "one buffer of the largest KB fits");
 constexpr int kThreads = 384;                   // producer, MMA, 2 spare, 8 epilogue warps
 constexpr int kEpiWarp0 = 4;                     // warps 4..11
 // Registers a thread: at launch, and after the quant phase for warpgroup 0
@@ -141,6 +145,46 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// A tile's scales into shared memory, by `nthr` threads (this one is `idx`):
+// the activation scales of its `rows` rows ([rows][KB], contiguous at src)
+// kb-major with rows padded to BM + 1 (so the epilogue's reads, [kb][its row],
+// hit distinct banks; rows past M read as 0), and the weight-block scales of
+// its two 128-column blocks nb0, nb0 + 1 ([2][KB]).  Coalesced 16-byte loads,
+// four in flight a thread, when the scale array is 16-byte aligned.
+__device__ __forceinline__ void stage_scales(float* asb, float* wsb, const float* src, int rows, const float* ws,
+                                             int nb0, int NB, int KB, int idx, int nthr) {
+    const int nv = rows * KB;
+    const int nv4 = ((reinterpret_cast<uintptr_t>(src) & 15) == 0) ? nv / 4 : 0;
+    for (int i0 = 0; i0 < nv4; i0 += 4 * nthr) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * nthr + idx;
+            v[u] = (i < nv4) ? reinterpret_cast<const float4*>(src)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * nthr + idx;
+            if (i < nv4) {
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int e = 4 * i + c, r = e / KB;
+                    asb[(e - r * KB) * (BM + 1) + r] = f[c];
+                }
+            }
+        }
+    }
+    for (int e = nv4 * 4 + idx; e < BM * KB; e += nthr) {      // the rest, then rows past M
+        const int r = e / KB;
+        asb[(e - r * KB) * (BM + 1) + r] = (e < nv) ? src[e] : 0.0f;
+    }
+    for (int e = idx; e < 2 * KB; e += nthr) {
+        const int h = e / KB, nb = nb0 + h;
+        wsb[e] = (nb < NB) ? ws[(int64_t)nb * KB + (e - h * KB)] : 0.0f;
+    }
+}
+
 // bounded wait for `need` quantised rows of m-tile mt
 __device__ __forceinline__ bool wait_rows(const int* ready, int need) {
     for (uint32_t i = 0; i < (1u << 22); ++i) {
@@ -164,19 +208,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = smem;                                        // kStages x 48 KB
     uint8_t* outst = smem + kStages * kTcStageBytes;             // output staging
     float* as_s = reinterpret_cast<float*>(outst + kOutBytes);   // [BM][KB + 1]
-    float* ws_s = as_s + BM * (kMaxKB + 1);                      // [2][KB]
+    float* ws_s = as_s + BM * (kMaxKB + 1);                      // [nsbuf][2][KB]
     uint64_t* bars = reinterpret_cast<uint64_t*>(ws_s + 2 * kMaxKB);
     uint64_t* full = bars;                                       // [kStages]
     uint64_t* empty = bars + kStages;                            // [kStages]
     uint64_t* tfull = bars + 2 * kStages;                        // [2] partial ready in TMEM
     uint64_t* tempty = bars + 2 * kStages + 2;                   // [2] partial consumed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    uint64_t* staged = bars + 2 * kStages + 4;                   // [2] a tile's scales are in smem
+    uint64_t* consumed = bars + 2 * kStages + 6;                 // [2] ... and no longer needed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
     int* flags = reinterpret_cast<int*>(tmem_slot + 2);          // [0] error, [1] ring issued, [2] mma k-blocks
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int total = p.mtiles * p.ntiles;
     const int KB = p.KB;
     const bool fused = p.a != nullptr;
+    const int nsbuf = KB <= kAsDoubleMaxKB ? 2 : 1;             // scale buffers
     volatile int* vflags = flags;
     auto fail = [&]() {
         record_error(p.err, kErrTimeout);
@@ -191,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 8);                            // one arrive per epilogue warp
+            mbar_init(&staged[b], 2);                            // one arrive per staging warp
+            mbar_init(&consumed[b], 8);                          // one arrive per epilogue warp
         }
         flags[0] = flags[1] = flags[2] = 0;
         fence_proxy_async_smem();
@@ -322,7 +371,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // warps 2..3: only the quant phase
+        if (warp >= 2) {
+            // ---------------- scale staging (warps 2..3) ----------------
+            // From this CTA's second tile on (the epilogue stages the first
+            // itself): once a tile's rows are quantised and its buffer is
+            // free, copy its scales into that buffer.
+            int j = 1;
+            for (int t = blockIdx.x + gridDim.x; t < total; t += gridDim.x, ++j) {
+                const int b = j % nsbuf;
+                const int mt = t / p.ntiles, nt = t % p.ntiles;
+                if (j >= nsbuf && *vflags == 0 &&
+                    !mbar_wait_sleep(&consumed[b], (uint32_t)(j / nsbuf - 1) & 1u))
+                    fail();
+                const int rows = min(BM, p.M - mt * BM);
+                if (fused && *vflags == 0 && !wait_rows(p.ready + mt, rows)) fail();
+                stage_scales(as_s + b * KB * (BM + 1), ws_s + b * 2 * KB, p.as + (int64_t)mt * BM * KB, rows, p.ws,
+                             nt * 2, p.NB, KB, (warp - 2) * 32 + lane, 64);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&staged[b]);
+            }
+        }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         // ---------------- epilogue: promotion + store ----------------
@@ -330,40 +398,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = ew >> 2;                   // column half
         const int q = warp & 3;                   // TMEM lane quarter of this warp
         const int rl = q * 32 + lane;             // row within the tile
-        const int wtid = ew * 32 + lane - wg * 128;   // 0..127 within the warpgroup
         const bool leader = (ew & 3) == 0 && lane == 0;
         uint8_t* stg = outst + wg * (128 * 128);
-        float* as_row = as_s + rl * (KB + 1);
-        float* ws_wg = ws_s + wg * KB;
-        int it = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int it = 0, j = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
             const int mt = t / p.ntiles, nt = t % p.ntiles;
-            const int nb = nt * 2 + wg;
-            const int64_t row = (int64_t)mt * BM + rl;
-            const bool row_ok = row < p.M;
-            // the scales of this m-tile come from the quant warps (of any CTA):
-            // wait (bounded, acquire) until all its rows are in
-            if (fused && *vflags == 0 && !wait_rows(p.ready + mt, min(BM, p.M - mt * BM))) fail();
-            // stage this tile's scales: my row's activation scales, my
-            // warpgroup's weight-block scales (all loads in flight together)
-            named_sync(1 + wg, 128);              // previous tile's readers are done
-            // this row's KB scales, 16 loads in flight at a time
-            for (int k0 = 0; k0 < KB; k0 += 16) {
-                float tmp[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) tmp[j] = (row_ok && k0 + j < KB) ? p.as[row * KB + k0 + j] : 0.0f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (k0 + j < KB) as_row[k0 + j] = tmp[j];
+            const int sb = j % nsbuf;
+            if (j == 0) {
+                // the first tile's scales: all 256 epilogue threads copy them
+                // (one round of loads), then stand in for the staging warps
+                const int rows = min(BM, p.M - mt * BM);
+                if (fused && *vflags == 0 && !wait_rows(p.ready + mt, rows)) fail();
+                stage_scales(as_s, ws_s, p.as + (int64_t)mt * BM * KB, rows, p.ws, nt * 2, p.NB, KB, ew * 32 + lane,
+                             256);
+                named_sync(3, 256);
+                if ((ew == 0 || ew == 4) && lane == 0) mbar_arrive(&staged[0]);
             }
-            for (int kb = wtid; kb < KB; kb += 128) ws_wg[kb] = (nb < p.NB) ? p.ws[(int64_t)nb * KB + kb] : 0.0f;
-            named_sync(1 + wg, 128);
+            // this tile's scales, from the staging warps
+            if (*vflags == 0 && !mbar_wait_sleep(&staged[sb], (uint32_t)(j / nsbuf) & 1u)) fail();
+            const float* as_col = as_s + sb * KB * (BM + 1) + rl;     // [kb * (BM + 1)]
+            const float* ws_wg = ws_s + sb * 2 * KB + wg * KB;
             float acc[128];
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int ab = it & 1;
-                const float sc = as_row[kb] * ws_wg[kb];
+                const float sc = as_col[kb * (BM + 1)] * ws_wg[kb];
                 if (*vflags == 0 && !mbar_wait_sleep(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
@@ -382,6 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&consumed[sb]);     // scale buffer free for a later tile
             // ---- bf16 out: two 64-column boxes through the swizzled staging, TMA stores ----
             const int col0 = nt * BN + wg * 128;
 #pragma unroll
