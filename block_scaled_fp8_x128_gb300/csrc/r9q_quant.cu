@@ -37,33 +37,54 @@ cudaError_t launch_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, cudaStre
 
 // ------------------------------------------------------ group-128 quant --
 
-// One warp per (token, group): lane l loads x[4l .. 4l+3] (8 bytes, the warp
-// reads the group's 256 bytes in one coalesced request), reduces amax with
-// shuffles, writes 4 codes; lane 0 writes the scale.
+// Four groups per warp step, eight lanes per group (lane l: 16 values of group
+// l >> 3, see quant_group128_lane8); a warp takes 16 consecutive groups of the
+// flattened [M][KB] group array per iteration, all loads in flight before any
+// is quantised.  K is a multiple of 128, so groups never straddle rows.
+constexpr int kQGroupsPerWarp = 16;
+
 __global__ void __launch_bounds__(256) quant_group128_kernel(const uint16_t* __restrict__ x, int64_t M,
                                                              int64_t K, uint8_t* __restrict__ xq,
                                                              float* __restrict__ xs) {
-    const int64_t KB = K / kBlock;
-    const int64_t groups = M * KB;
+    const int64_t groups = M * (K / kBlock);
     const int lane = threadIdx.x & 31;
+    const int gl = lane >> 3, el = (lane & 7) * 16;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t g = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; g < groups; g += warps) {
-        const int64_t m = g / KB, kb = g % KB;
-        const int64_t off = m * K + kb * kBlock + 4 * lane;
-        const uint2 v = *reinterpret_cast<const uint2*>(x + off);
-        float s;
-        const uint32_t codes =
-            quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s);
-        *reinterpret_cast<uint32_t*>(xq + off) = codes;
-        if (lane == 0) xs[g] = s;
+    for (int64_t g0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kQGroupsPerWarp; g0 < groups;
+         g0 += warps * kQGroupsPerWarp) {
+        uint4 v[kQGroupsPerWarp / 4][2];
+#pragma unroll
+        for (int j = 0; j < kQGroupsPerWarp / 4; ++j) {
+            const int64_t g = g0 + 4 * j + gl;
+            if (g < groups) {
+                const uint4* q = reinterpret_cast<const uint4*>(x + g * kBlock + el);
+                v[j][0] = q[0];
+                v[j][1] = q[1];
+            } else {
+                v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kQGroupsPerWarp / 4; ++j) {
+            if (g0 + 4 * j < groups) {
+                const int64_t g = g0 + 4 * j + gl;
+                float sc;
+                const uint4 codes = quant_group128_lane8(v[j], sc);
+                if (g < groups) {
+                    *reinterpret_cast<uint4*>(xq + g * kBlock + el) = codes;
+                    if ((lane & 7) == 0) xs[g] = sc;
+                }
+            }
+        }
     }
 }
 
 cudaError_t launch_quant_group128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,
                                   cudaStream_t st, int sms) {
     const int64_t groups = M * (K / kBlock);
-    int64_t blocks = (groups + 7) / 8;
-    const int64_t cap = (int64_t)sms * 16;
+    const int64_t per_block = 8 * kQGroupsPerWarp;                 // 8 warps
+    int64_t blocks = (groups + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sms * 4;                           // 32 warps an SM
     int grid = (int)(blocks < cap ? blocks : cap);
     quant_group128_kernel<<<grid, 256, 0, st>>>(x, M, K, xq, xs);
     return cudaGetLastError();

@@ -263,46 +263,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         // published to its m-tile's ready counter.
         const int gw = blockIdx.x * (kThreads / 32) + warp;
         const int GW = gridDim.x * (kThreads / 32);
-        for (int64_t row = gw; row < p.M; row += GW) {
+        // A warp's rows are a stream of 16-group chunks; the next chunk's
+        // loads are issued before the current chunk is quantised.  Lane l
+        // holds 16 values of group 4j + (l >> 3) of the chunk.
+        constexpr int CH = 16;
+        const int nch = (KB + CH - 1) / CH;
+        const int gl = lane >> 3, el = (lane & 7) * 16;
+        auto load = [&](uint4 (&v)[CH / 4][2], int64_t row, int c) {
             const uint16_t* src = p.a + row * p.K;
+#pragma unroll
+            for (int j = 0; j < CH / 4; ++j) {
+                const int g = c * CH + 4 * j + gl;
+                if (g < KB) {
+                    const uint4* q = reinterpret_cast<const uint4*>(src + (int64_t)g * BK + el);
+                    v[j][0] = q[0];
+                    v[j][1] = q[1];
+                } else {
+                    v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        };
+        auto quant = [&](const uint4 (&v)[CH / 4][2], int64_t row, int c) {
             uint8_t* dq = p.aq + row * p.K;
-            // this warp's next row goes to L2 while this one is quantised
-            if (lane == 0 && row + GW < p.M) bulk_prefetch_l2(src + (int64_t)GW * p.K, (uint32_t)(2 * p.K));
-            // four groups per step (eight lanes each, 16 values a lane); the
-            // whole chunk of up to 32 groups is loaded before any is quantised
-            constexpr int CH = 32;
-            const int gl = lane >> 3, el = (lane & 7) * 16;
-            for (int g0 = 0; g0 < KB; g0 += CH) {
-                uint4 v[CH / 4][2];
 #pragma unroll
-                for (int j = 0; j < CH / 4; ++j) {
-                    const int g = g0 + 4 * j + gl;
+            for (int j = 0; j < CH / 4; ++j) {
+                if (c * CH + 4 * j < KB) {
+                    const int g = c * CH + 4 * j + gl;
+                    float sc;
+                    const uint4 codes = quant_group128_lane8(v[j], sc);
                     if (g < KB) {
-                        const uint4* q = reinterpret_cast<const uint4*>(src + (int64_t)g * BK + el);
-                        v[j][0] = q[0];
-                        v[j][1] = q[1];
-                    } else {
-                        v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < CH / 4; ++j) {
-                    if (g0 + 4 * j < KB) {
-                        const int g = g0 + 4 * j + gl;
-                        float sc;
-                        const uint4 codes = quant_group128_lane8(v[j], sc);
-                        if (g < KB) {
-                            *reinterpret_cast<uint4*>(dq + (int64_t)g * BK + el) = codes;
-                            if ((lane & 7) == 0) p.as[row * KB + g] = sc;
-                        }
+                        *reinterpret_cast<uint4*>(dq + (int64_t)g * BK + el) = codes;
+                        if ((lane & 7) == 0) p.as[row * KB + g] = sc;
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) {
-                fence_proxy_async_global();
-                red_release_add(p.ready + row / BM, 1);
+            if (c == nch - 1) {
+                // the row is done: publish it to its m-tile's ready counter
+                __syncwarp();
+                if (lane == 0) {
+                    fence_proxy_async_global();
+                    red_release_add(p.ready + row / BM, 1);
+                }
             }
+        };
+        auto next = [&](int64_t& row, int& c) {
+            if (++c == nch) {
+                c = 0;
+                row += GW;
+            }
+        };
+        uint4 va[CH / 4][2], vb[CH / 4][2];
+        int64_t row = gw;
+        int c = 0;
+        if (row < p.M) load(va, row, c);
+        while (row < p.M) {
+            // this warp's next row goes to L2 while this one is quantised
+            if (c == 0 && lane == 0 && row + GW < p.M)
+                bulk_prefetch_l2(p.a + (row + GW) * p.K, (uint32_t)(2 * p.K));
+            int64_t row2 = row;
+            int c2 = c;
+            next(row2, c2);
+            if (row2 < p.M) load(vb, row2, c2);
+            quant(va, row, c);
+            row = row2;
+            c = c2;
+            if (row >= p.M) break;
+            if (c == 0 && lane == 0 && row + GW < p.M)
+                bulk_prefetch_l2(p.a + (row + GW) * p.K, (uint32_t)(2 * p.K));
+            next(row2, c2);
+            if (row2 < p.M) load(va, row2, c2);
+            quant(vb, row, c);
+            row = row2;
+            c = c2;
         }
     }
 
