@@ -427,6 +427,14 @@ def profile_case(case, calls):
     import block_scaled_fp8_x128_gb300 as r9q
     import synth
     dev = torch.device("cuda", 0)
+    if case == "quant-8192":
+        M, K = 8192, 4096
+        X = [torch.from_numpy(synth.to_bf16_bits(synth.activations(4, M, K)).view(np.int16)).view(torch.bfloat16).to(dev)
+             for _ in range(4)]
+        for i in range(calls):
+            r9q.r9q_quant_group128(X[i % 4])
+        torch.cuda.synchronize()
+        return
     if case == "c3":
         M, H, I, Ho = 8, 4096, 1536, 4096
         x = torch.from_numpy(synth.to_bf16_bits(synth.activations(3, M, H)).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -484,7 +492,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     ap.add_argument("--no-pdl", action="store_true", help="launch every GEMM fully serialised")
-    ap.add_argument("--profile-case", choices=["c1", "c4-8192", "c2-16", "c3"], default=None,
+    ap.add_argument("--profile-case", choices=["c1", "c4-8192", "c2-16", "c3", "quant-8192"], default=None,
                     help="only run a few calls of one workload (for an external profiler) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
