@@ -213,7 +213,9 @@ def test_w8a8_c4_prefill_sampled(r9q):
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 256, 384), (5, 384, 640), (13, 128, 128), (17, 640, 256),
-                                   (33, 256, 1152), (63, 384, 512), (65, 256, 512), (100, 128, 384)])
+                                   (33, 256, 1152), (63, 384, 512), (65, 256, 512), (100, 128, 384),
+                                   (130, 384, 5120),     # tensor-core path, 3-stage ring, two scale buffers
+                                   (200, 256, 8192)])    # ... one scale buffer
 def test_w8a8_ragged(r9q, M, N, K):
     _w8a8_case(r9q, M, N, K, 0.01, 20.0, 11)
 
