@@ -30,6 +30,7 @@ _SIGS = {
     "r9q_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "r9q_last_device_error": ([_P], ctypes.c_int),
     "r9q_set_pdl": ([ctypes.c_int], ctypes.c_int),
+    "r9q_selftest_wait_timeout": ([ctypes.c_int, _P], ctypes.c_int),
     "r9q_e4m3_from_f32": ([_P, _I64, _P, _P], ctypes.c_int),
     "r9q_quant_group128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "r9q_quant_weight_block128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
@@ -49,6 +50,7 @@ for _name, (_args, _res) in _SIGS.items():
 
 EXPORTED = tuple(_SIGS)
 
+R9Q_ERR_TIMEOUT = -6
 R9Q_MLP_WEIGHT_ONLY = 1
 R9Q_MLP_UNFUSED = 2
 R9Q_OP_GEMM_W8A8 = 1
@@ -97,6 +99,12 @@ def r9q_version() -> int:
 
 def r9q_strerror(code: int) -> str:
     return _lib.r9q_strerror(int(code)).decode()
+
+
+def r9q_selftest_wait_timeout(which: int, stream=None) -> None:
+    """Launch the failure-detection self-test kernel (its bounded waits run
+    out and record R9Q_ERR_TIMEOUT; read it with r9q_last_device_error)."""
+    _check(_lib.r9q_selftest_wait_timeout(int(which), _stream(stream)), "r9q_selftest_wait_timeout")
 
 
 def r9q_set_pdl(enable: bool) -> bool:

@@ -320,6 +320,15 @@ int run_stream_gemm(int amode, int epi, const void* a, uint8_t* aq, float* as, c
 }
 
 }  // namespace
+
+int device_error_word(int** out) {
+    DeviceInfo* d = nullptr;
+    const int rc = current_device(&d);
+    if (rc) return rc;
+    *out = d->err;
+    return R9Q_OK;
+}
+
 }  // namespace r9q
 
 using namespace r9q;

@@ -9,7 +9,12 @@
 namespace r9q {
 
 constexpr int kBlock = 128;                 // scale block edge (K group and weight block)
-constexpr uint32_t kSpinLimit = 1u << 22;   // bounded waits: ~0.3 s with back-off, then error
+// Bounds of the device waits (then an error is recorded and the kernel
+// returns): an mbarrier try_wait without a hint suspends for ~3.7 us in
+// hardware when the phase is not complete, so 2^18 tries last ~1 s; a counter
+// poll with a 128 ns sleep takes ~0.2 us, so 2^22 polls last ~1 s.
+constexpr uint32_t kSpinLimit = 1u << 18;
+constexpr uint32_t kCountSpinLimit = 1u << 22;
 constexpr int kErrTimeout = -6;             // R9Q_ERR_TIMEOUT
 
 // ------------------------------------------------------------------ basics --
@@ -227,6 +232,21 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     for (uint32_t i = 0; i < kSpinLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Bounded wait (acquire, gpu scope) until *counter >= need; false after
+// about a second.
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool wait_count(const int* counter, int need) {
+    for (uint32_t i = 0; i < kCountSpinLimit; ++i) {
+        if (ld_acquire(counter) >= need) return true;
+        __nanosleep(128);
+    }
     return false;
 }
 

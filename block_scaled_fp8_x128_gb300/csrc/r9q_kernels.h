@@ -69,6 +69,9 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
                            const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
                            int K, int* err, int sms, cudaStream_t st);
 
+// The current device's error word (kernels record bounded-wait timeouts there).
+int device_error_word(int** out);
+
 // ---- elementwise / quantisation ----
 cudaError_t launch_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, cudaStream_t st, int sms);
 cudaError_t launch_quant_group128(const uint16_t* x, int64_t M, int64_t K, uint8_t* xq, float* xs,

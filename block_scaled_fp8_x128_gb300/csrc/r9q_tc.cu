@@ -133,11 +133,6 @@ __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ void red_release_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -186,13 +181,7 @@ __device__ __forceinline__ void stage_scales(float* asb, float* wsb, const float
 }
 
 // bounded wait for `need` quantised rows of m-tile mt
-__device__ __forceinline__ bool wait_rows(const int* ready, int need) {
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (ld_acquire(ready) >= need) return true;
-        __nanosleep(128);
-    }
-    return false;
-}
+__device__ __forceinline__ bool wait_rows(const int* ready, int need) { return wait_count(ready, need); }
 
 }  // namespace tc
 

@@ -70,6 +70,19 @@ const char* r9q_strerror(int code);
  * otherwise the recorded negative code (R9Q_ERR_TIMEOUT). */
 int r9q_last_device_error(void* stream);
 
+/* Failure-detection self-test; the pages have no counterpart.  Launches one
+ * small kernel on `stream` whose bounded device waits run out, each on an
+ * mbarrier or a counter that nothing ever completes: `which` is a bit set of
+ * 1 = the spinning mbarrier wait of the GEMM pipelines, 2 = the sleeping one,
+ * 4 = the cluster-scope wait of the split-K reduction, 8 = the counter wait on
+ * the prefill kernel's quantised-row counters.  Each selected wait gives up
+ * after its bound (up to about a second), the kernel records R9Q_ERR_TIMEOUT
+ * in the device error word and returns, and the context stays usable; read
+ * the word with r9q_last_device_error.  which = 0 runs the kernel with no
+ * wait (nothing is recorded).  Returns R9Q_ERR_ARG for `which` outside 0..15,
+ * R9Q_ERR_LAUNCH if the launch fails, else R9Q_OK. */
+int r9q_selftest_wait_timeout(int which, void* stream);
+
 /* Programmatic dependent launch of the GEMM entry points (default: off).
  * When on, a GEMM kernel may begin while the kernel launched just before it on
  * the same stream is still running: it starts streaming its weights w at once

@@ -357,6 +357,28 @@ def test_device_error_word_clear(r9q):
     assert r9q.r9q_last_device_error() == 0
 
 
+def test_selftest_without_waits_records_nothing(r9q):
+    assert r9q.r9q_last_device_error() == 0
+    r9q.r9q_selftest_wait_timeout(0)
+    assert r9q.r9q_last_device_error() == 0
+
+
+@pytest.mark.parametrize("which", [1, 2, 4, 8])
+def test_bounded_wait_runs_out_and_context_survives(r9q, which):
+    """A wait on an mbarrier / counter that nothing completes gives up within
+    its bound, the host reads R9Q_ERR_TIMEOUT (once), and the next GEMM on the
+    same context is correct."""
+    import time
+    assert r9q.r9q_last_device_error() == 0
+    t0 = time.perf_counter()
+    r9q.r9q_selftest_wait_timeout(which)
+    assert r9q.r9q_last_device_error() == r9q.R9Q_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 30.0
+    assert r9q.r9q_last_device_error() == 0
+    _w8a8_case(r9q, 5, 384, 640, 0.01, 20.0, 11)
+    assert r9q.r9q_last_device_error() == 0
+
+
 def test_pdl_dependent_chain_matches_serialised(r9q):
     """With programmatic launch on, a GEMM whose activations are the previous
     GEMM's output must still see that output: a 6-deep chain, PDL on vs off."""

@@ -87,6 +87,15 @@ def test_host_argument_checks(lib):
     assert g(*base, 8, 256, 200, 256, None, None, None, 0, None, 0, None) == c["R9Q_ERR_DIM"]
 
 
+def test_selftest_rejects_unknown_waits(lib):
+    c = _codes()
+    f = lib.r9q_selftest_wait_timeout
+    f.argtypes = [ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(16, None) == c["R9Q_ERR_ARG"]
+    assert f(-1, None) == c["R9Q_ERR_ARG"]
+
+
 def test_workspace_query(lib):
     c = _codes()
     f = lib.r9q_workspace_bytes
