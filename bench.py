@@ -367,6 +367,38 @@ def sweep(torch, r9q, stream, hbm, fp8_peak, src):
         res.append({"config": "c3", "mode": f"expert MLP W8A8 ({label})", "M": M, "H": H, "I": I, "H_out": Ho,
                     "us_per_call": round(us, 3), "GBps": round(bpc / us / 1e3, 1),
                     "frac_hbm": round(bpc / us / 1e3 / hbm, 4)})
+    del WG, WD, HB, YB
+    torch.cuda.empty_cache()
+
+    # MoE decode layer: E experts with T tokens each (the c3 expert shape), grouped
+    # gate_up (SwiGLU epilogue) + grouped down (fused quant of h): two launches,
+    # against E separate fused expert-MLP calls.  Every expert has its own weight
+    # copy (same values), rotated over copies > 3x L2.
+    E, T = 8, 8
+    bpc_e = E * bpc
+    copies_e = _copies_for(bpc_e)
+    xe = torch.from_numpy(synth.to_bf16_bits(synth.activations(3, E * T, H)).view(np.int16)).view(torch.bfloat16).to(dev)
+    GU = [torch.stack([wgu] * E).clone() for _ in range(copies_e)]
+    DN = [torch.stack([wdn] * E).clone() for _ in range(copies_e)]
+    SGU, SDN = torch.stack([sgu] * E), torch.stack([sdn] * E)
+    he = torch.empty((E * T, I), dtype=torch.bfloat16, device=dev)
+    ye = torch.empty((E * T, Ho), dtype=torch.bfloat16, device=dev)
+    off = [T * e for e in range(E + 1)]
+    torch.cuda.synchronize()
+
+    def grouped(i):
+        r9q.r9q_grouped_gemm_fp8(xe, off, GU[i], SGU, y=he, flags=r9q.R9Q_GROUPED_SWIGLU)
+        r9q.r9q_grouped_gemm_fp8(he, off, DN[i], SDN, y=ye)
+
+    def per_expert(i):
+        for e in range(E):
+            r9q.r9q_gate_up_swiglu_down(xe[T * e:T * (e + 1)], GU[i][e], sgu, DN[i][e], sdn,
+                                        y=ye[T * e:T * (e + 1)], h=he[T * e:T * (e + 1)])
+    for fn, label in ((grouped, "grouped, 2 launches"), (per_expert, f"{E} fused expert-MLP calls")):
+        us = timeit(fn, copies_e, 500)
+        res.append({"config": "moe", "mode": f"MoE decode layer W8A8, {E} experts x {T} tokens ({label})",
+                    "E": E, "T": T, "H": H, "I": I, "H_out": Ho, "us_per_call": round(us, 3),
+                    "GBps": round(bpc_e / us / 1e3, 1), "frac_hbm": round(bpc_e / us / 1e3 / hbm, 4)})
     return res
 
 

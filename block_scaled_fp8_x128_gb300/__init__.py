@@ -31,6 +31,8 @@ _SIGS = {
     "r9q_last_device_error": ([_P], ctypes.c_int),
     "r9q_set_pdl": ([ctypes.c_int], ctypes.c_int),
     "r9q_selftest_wait_timeout": ([ctypes.c_int, _P], ctypes.c_int),
+    "r9q_grouped_gemm_fp8": ([_P, ctypes.POINTER(_I64), _I64, _P, _P, _P, _I64, _I64, ctypes.c_int, _P],
+                             ctypes.c_int),
     "r9q_e4m3_from_f32": ([_P, _I64, _P, _P], ctypes.c_int),
     "r9q_quant_group128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "r9q_quant_weight_block128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
@@ -51,6 +53,8 @@ for _name, (_args, _res) in _SIGS.items():
 EXPORTED = tuple(_SIGS)
 
 R9Q_ERR_TIMEOUT = -6
+R9Q_GROUPED_WEIGHT_ONLY = 1
+R9Q_GROUPED_SWIGLU = 2
 R9Q_MLP_WEIGHT_ONLY = 1
 R9Q_MLP_UNFUSED = 2
 R9Q_OP_GEMM_W8A8 = 1
@@ -99,6 +103,30 @@ def r9q_version() -> int:
 
 def r9q_strerror(code: int) -> str:
     return _lib.r9q_strerror(int(code)).decode()
+
+
+def r9q_grouped_gemm_fp8(a: torch.Tensor, offsets, w: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | None = None,
+                         flags: int = 0, stream=None) -> torch.Tensor:
+    """Several experts in one launch: a bf16 [offsets[-1]][K] (tokens sorted by
+    expert), offsets host ints [E + 1], w e4m3 [E][N][K], ws fp32
+    [E][N/128][K/128]; y bf16 [offsets[-1]][N] (N/2 with R9Q_GROUPED_SWIGLU)."""
+    off = [int(v) for v in offsets]
+    E = len(off) - 1
+    Mtot, K = a.shape
+    _expect(a, torch.bfloat16, (off[-1], K), "a")
+    if w.dim() != 3 or w.shape[0] != E or w.shape[2] != K:
+        raise ValueError("w must be [E][N][K]")
+    N = w.shape[1]
+    _expect(w, torch.uint8, (E, N, K), "w")
+    _expect(ws, torch.float32, (E, N // 128, K // 128), "ws")
+    ncols = N // 2 if flags & R9Q_GROUPED_SWIGLU else N
+    if y is None:
+        y = torch.empty((Mtot, ncols), dtype=torch.bfloat16, device=a.device)
+    _expect(y, torch.bfloat16, (Mtot, ncols), "y")
+    arr = (_I64 * (E + 1))(*off)
+    _check(_lib.r9q_grouped_gemm_fp8(_ptr(a), arr, E, _ptr(w), _ptr(ws), _ptr(y), N, K, int(flags), _stream(stream)),
+           "r9q_grouped_gemm_fp8")
+    return y
 
 
 def r9q_selftest_wait_timeout(which: int, stream=None) -> None:

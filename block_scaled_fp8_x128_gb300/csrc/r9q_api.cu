@@ -406,6 +406,69 @@ int r9q_quant_weight_block128(const float* w, int64_t N, int64_t K, uint8_t* wq,
     return to_status(launch_quant_weight_block128(w, N, K, wq, ws, static_cast<cudaStream_t>(stream)));
 }
 
+int r9q_grouped_gemm_fp8(const void* a_bf16, const int64_t* offsets, int64_t E, const uint8_t* w, const float* ws,
+                         void* y_bf16, int64_t N, int64_t K, int flags, void* stream) {
+    if (flags & ~(R9Q_GROUPED_WEIGHT_ONLY | R9Q_GROUPED_SWIGLU)) return R9Q_ERR_ARG;
+    if (!offsets) return R9Q_ERR_NULL;
+    if (E < 1 || E > kMaxGroups) return R9Q_ERR_DIM;
+    if (offsets[0] != 0) return R9Q_ERR_ARG;
+    int64_t max_m = 0;
+    int active = 0;
+    for (int64_t g = 0; g < E; ++g) {
+        const int64_t m = offsets[g + 1] - offsets[g];
+        if (m < 0) return R9Q_ERR_ARG;
+        if (m > max_m) max_m = m;
+        active += m > 0;
+    }
+    const int64_t Mtot = offsets[E];
+    if (Mtot > INT_MAX) return R9Q_ERR_DIM;
+    if (Mtot == 0) return R9Q_OK;                          // no token routed anywhere
+    if (!a_bf16 || !w || !ws || !y_bf16) return R9Q_ERR_NULL;
+    const bool swiglu = flags & R9Q_GROUPED_SWIGLU;
+    int rc = check_mnk(Mtot, N, K);
+    if (rc) return rc;
+    if (swiglu && N % 256) return R9Q_ERR_DIM;
+    if (E * N > INT_MAX) return R9Q_ERR_DIM;
+    if (!aligned(a_bf16, 16) || !aligned(w, 16) || !aligned(y_bf16, 16) || !aligned(ws, 4)) return R9Q_ERR_ALIGN;
+    const int64_t ncols = swiglu ? N / 2 : N;
+    const size_t ybytes = 2 * (size_t)(Mtot * ncols);
+    if (overlaps(y_bf16, ybytes, a_bf16, 2 * (size_t)(Mtot * K)) || overlaps(y_bf16, ybytes, w, (size_t)(E * N * K)))
+        return R9Q_ERR_ARG;
+    DeviceInfo* d = nullptr;
+    rc = current_device(&d);
+    if (rc) return rc;
+    const int amode = (flags & R9Q_GROUPED_WEIGHT_ONLY) ? A_BF16 : A_QUANT;
+    // One expert's GEMM planned as if it had its share of the SMs.
+    StreamPlan plan;
+    const int share = d->sms / active > 0 ? d->sms / active : 1;
+    if (!plan_stream(max_m, N, K, amode, share, &plan)) return R9Q_ERR_DIM;
+    GroupTable gt;
+    gt.zchunks = (int)((max_m + plan.MT - 1) / plan.MT);
+    gt.wrows = (int)N;
+    for (int64_t g = 0; g <= E; ++g) gt.off[g] = (int)offsets[g];
+    if ((int64_t)E * gt.zchunks > 65535) return R9Q_ERR_DIM;
+    CUtensorMap tm;
+    rc = weight_tmap(w, E * N, K, &tm);
+    if (rc) return rc;
+    StreamParams p;
+    p.a = static_cast<const uint16_t*>(a_bf16);
+    p.aq = nullptr;
+    p.as = nullptr;
+    p.ws = ws;
+    p.y = static_cast<uint16_t*>(y_bf16);
+    p.M = (int)Mtot;
+    p.K = (int)K;
+    p.KB = (int)(K / 128);
+    p.ldy = (int)ncols;
+    p.splits = plan.splits;
+    p.groups = plan.groups;
+    p.ntiles = plan.ntiles;
+    p.stages = plan.stages;
+    p.err = d->err;
+    return to_status(launch_stream_grouped(plan, amode, swiglu ? EPI_SWIGLU : EPI_STORE, tm, p, gt, (int)E,
+                                           static_cast<cudaStream_t>(stream), g_pdl.load() != 0));
+}
+
 int r9q_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t N2, int flags, size_t* bytes) {
     if (!bytes) return R9Q_ERR_NULL;
     switch (op) {

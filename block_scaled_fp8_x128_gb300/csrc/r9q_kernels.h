@@ -34,6 +34,14 @@ struct StreamParams {
     int* err;            // device error word
 };
 
+// Expert table of the grouped launch (passed by value with the launch).
+constexpr int kMaxGroups = 128;
+struct GroupTable {
+    int zchunks;                 // token chunks (of MT rows) per expert in grid.z
+    int wrows;                   // weight rows per expert (N; 2I for the SwiGLU epilogue)
+    int off[kMaxGroups + 1];     // expert g's token rows: [off[g], off[g+1])
+};
+
 struct StreamPlan {
     int MT;              // token tile: 8, 16, 32 or 64
     int splits;          // cluster size along K
@@ -56,6 +64,11 @@ cudaError_t launch_stream_a_preq(const StreamPlan& plan, int epi, const CUtensor
                                  const StreamParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_stream_a_bf16(const StreamPlan& plan, int epi, const CUtensorMap& wmap,
                                  const StreamParams& p, cudaStream_t st, bool pdl);
+
+// Grouped launch (A_QUANT or A_BF16 A-loads): grid.z = experts x zchunks.
+cudaError_t launch_stream_grouped(const StreamPlan& plan, int amode, int epi, const CUtensorMap& wmap,
+                                  const StreamParams& p, const GroupTable& gt, int nexperts, cudaStream_t st,
+                                  bool pdl);
 
 // Raises a kernel's dynamic shared memory limit once per device (the attribute
 // is not touched again afterwards, so launches can be captured in graphs).

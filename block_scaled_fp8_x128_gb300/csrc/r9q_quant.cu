@@ -1,8 +1,8 @@
 // Standalone quantisation kernels of libr9q (sm_103a):
 //   * fp32 -> e4m3 conversion (the codec every quantiser uses),
 //   * per-token-group-128 activation quantisation (the separate pass of the
-//     unfused W8A8 path; r9700-stack v0.3.1 notes, fused activation quant
-//     "=0 splits it again"),
+//     unfused W8A8 path; r9700-stack v0.3.1 notes: what runs when the fused
+//     activation quant is switched off),
 //   * weight quantisation with one fp32 scale per 128x128 block (set-up),
 //   * the SwiGLU of the separate-launch expert MLP chain (releases page,
 //     v0.3.3 "What changed": the three-launch path the fused one must match).

@@ -86,9 +86,12 @@ __device__ __forceinline__ void tile_rows(int t, int& r0, int& r1, int& nb0, int
     }
 }
 
+// The kernel body for the token rows [m0, m0 + mvalid) (mvalid >= 1) of one
+// problem whose weight rows start at wrow0 and whose block-scale rows start at
+// nbase (both 0 for a single GEMM; an expert's offsets in the grouped launch).
 template <int MT, int AMODE, int EPI>
-__global__ void __launch_bounds__(kStreamThreads)
-    stream_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p) {
+__device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const StreamParams& p, const int m0,
+                                                 const int mvalid, const int wrow0, const int nbase) {
     constexpr int NT = MT / 8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -100,8 +103,6 @@ __global__ void __launch_bounds__(kStreamThreads)
     const int S = p.splits, G = p.groups, nst = p.stages;
     const int split = (int)cluster_ctarank();
     const int group = blockIdx.y;
-    const int m0 = blockIdx.z * MT;
-    const int mvalid = min(MT, p.M - m0);
     const int KB = p.KB;
     const int kbase = KB / S, krem = KB % S;
     const int kb0 = split * kbase + min(split, krem);
@@ -167,6 +168,8 @@ __global__ void __launch_bounds__(kStreamThreads)
             const int tl = it / nkb, i = it - tl * nkb;
             int r0, r1, nb0, nb1;
             tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
+            r0 += wrow0;
+            r1 += wrow0;
             mbar_expect_tx(&full[it], kStageBytes);
             tma_load_2d(ring + it * kStageBytes, &wmap, (kb0 + i) * kBlock, r0, &full[it]);
             tma_load_2d(ring + it * kStageBytes + kStageBytes / 2, &wmap, (kb0 + i) * kBlock, r1, &full[it]);
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(kStreamThreads)
             const int tl = it / nkb, i = it - tl * nkb;
             int r0, r1, nb0, nb1;
             tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
-            tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, r0);
-            tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, r1);
+            tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, wrow0 + r0);
+            tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, wrow0 + r1);
         }
     }
     // Weights and their block scales never come from the preceding kernel:
@@ -197,8 +200,8 @@ __global__ void __launch_bounds__(kStreamThreads)
         const int tl = c / nkb, i = c - tl * nkb;
         int r0, r1, nb0, nb1;
         tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
-        ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)nb0 * KB + kb0 + i];
-        ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)nb1 * KB + kb0 + i];
+        ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
+        ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
     }
     pdl_wait();
     if (producer) {
@@ -456,6 +459,8 @@ __global__ void __launch_bounds__(kStreamThreads)
             const int tl = it / nkb, i = it - tl * nkb;
             if (tl != cur_tl) {
                 tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
+                r0 += wrow0;
+                r1 += wrow0;
                 cur_tl = tl;
             }
             mbar_expect_tx(&full[st], kStageBytes);
@@ -474,6 +479,29 @@ __global__ void __launch_bounds__(kStreamThreads)
         for (int it = max(0, issued - nst); it < issued; ++it)
             (void)mbar_wait(&full[it % nst], (uint32_t)(it / nst) & 1u);
     }
+}
+
+template <int MT, int AMODE, int EPI>
+__global__ void __launch_bounds__(kStreamThreads)
+    stream_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p) {
+    const int m0 = blockIdx.z * MT;
+    stream_gemm_body<MT, AMODE, EPI>(wmap, p, m0, min(MT, p.M - m0), 0, 0);
+}
+
+// Grouped launch: grid.z = expert x token chunk; expert g owns the token rows
+// [off[g], off[g+1]), weight rows [g * wrows, (g+1) * wrows) and block-scale
+// rows [g * wrows/128, ...).  Chunks past an expert's tokens leave at once: the
+// cluster shares blockIdx.z, so all its CTAs leave together, before any
+// cluster barrier.
+template <int MT, int AMODE, int EPI>
+__global__ void __launch_bounds__(kStreamThreads)
+    stream_grouped_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p,
+                          const __grid_constant__ GroupTable gt) {
+    const int g = (int)blockIdx.z / gt.zchunks;
+    const int m0 = gt.off[g] + ((int)blockIdx.z - g * gt.zchunks) * MT;
+    const int mvalid = min(MT, gt.off[g + 1] - m0);
+    if (mvalid <= 0) return;
+    stream_gemm_body<MT, AMODE, EPI>(wmap, p, m0, mvalid, g * gt.wrows, g * (gt.wrows / kBlock));
 }
 
 template <int AMODE>

@@ -10,7 +10,7 @@
  *                 byte-identical to a separate quantisation pass
  *                 (r9700-stack v0.3.1 release notes, "What changed for someone
  *                 running it": fused activation quant in the dense fp8 block
- *                 GEMM, "=0 splits it again");
+ *                 GEMM, whose off setting restores the separate pass);
  *   weight-only — the fp8 weights against the unquantised bf16 activations
  *                 (same notes: fp8 hyper-connection decode GEMMs, bf16 MMA
  *                 against the unquantised activations).
@@ -70,6 +70,32 @@ const char* r9q_strerror(int code);
  * otherwise the recorded negative code (R9Q_ERR_TIMEOUT). */
 int r9q_last_device_error(void* stream);
 
+/* Grouped block-fp8 GEMM: several experts in one launch, for the MoE decode
+ * path (releases page, v0.3.3 "What changed": the fused MoE decode path),
+ * where each expert's GEMM has only a few tokens.  Expert g multiplies its
+ * token rows a[offsets[g] .. offsets[g+1]) by its own weights and writes the
+ * same rows of y; experts with no token cost nothing.  Per expert the
+ * operation is that of r9q_gemm_fp8_block_qa (W8A8 with the group-128
+ * activation quant in the A-load) or, with
+ * R9Q_GROUPED_WEIGHT_ONLY, that of r9q_gemm_fp8w_bf16a; with
+ * R9Q_GROUPED_SWIGLU the epilogue is that of the gate_up GEMM of
+ * r9q_gate_up_swiglu_down (gate/up rows interleaved per 128, h = silu(g)*u).
+ *   a_bf16   bf16 [offsets[E]][K], tokens sorted by expert (device)
+ *   offsets  int64 [E + 1] on the HOST: offsets[0] = 0, non-decreasing
+ *   E        1..128 experts
+ *   w        e4m3 [E][N][K] (device), expert g's weights at g*N*K
+ *   ws       fp32 [E][N/128][K/128] (device)
+ *   y_bf16   bf16 [offsets[E]][N], or [offsets[E]][N/2] with R9Q_GROUPED_SWIGLU
+ * N and K multiples of 128 (N of 256 with R9Q_GROUPED_SWIGLU); the fused quant
+ * writes no codes out.  Errors: R9Q_ERR_NULL, R9Q_ERR_DIM (sizes, E),
+ * R9Q_ERR_ARG (offsets not starting at 0 or decreasing, unknown flags, y
+ * overlapping an input), R9Q_ERR_ALIGN, R9Q_ERR_LAUNCH.  offsets[E] = 0 is a
+ * no-op.  Allocates nothing; asynchronous on `stream`. */
+#define R9Q_GROUPED_WEIGHT_ONLY 1
+#define R9Q_GROUPED_SWIGLU      2
+int r9q_grouped_gemm_fp8(const void* a_bf16, const int64_t* offsets, int64_t E, const uint8_t* w, const float* ws,
+                         void* y_bf16, int64_t N, int64_t K, int flags, void* stream);
+
 /* Failure-detection self-test; the pages have no counterpart.  Launches one
  * small kernel on `stream` whose bounded device waits run out, each on an
  * mbarrier or a counter that nothing ever completes: `which` is a bit set of
@@ -100,8 +126,8 @@ int r9q_set_pdl(int enable);
 int r9q_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, void* stream);
 
 /* Per-token-group-128 activation quantisation (the separate pass of the
- * unfused W8A8 path; r9700-stack v0.3.1 notes, fused activation quant "=0
- * splits it again").  x_bf16[M][K] -> xq[M][K] e4m3 codes and
+ * unfused W8A8 path; r9700-stack v0.3.1 notes: what runs when the fused
+ * activation quant is switched off).  x_bf16[M][K] -> xq[M][K] e4m3 codes and
  * xs[M][K/128] fp32 scales, s = amax/448 (fp32 division), q = e4m3(x/s) with
  * one fp32 division per element; an all-zero group gives s = 0 and codes 0. */
 int r9q_quant_group128(const void* x_bf16, int64_t M, int64_t K,

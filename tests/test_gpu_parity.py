@@ -260,6 +260,62 @@ def test_w8bf16_every_code_exact(r9q):
     assert len(seen) == 254        # all finite codes exercised
 
 
+# ------------------------------------------------------ grouped (experts) --
+
+def _grouped_case(r9q, counts, N, K, flags, seed):
+    """One launch over len(counts) experts; each expert's rows against the
+    oracle's GEMM on the same operands (W8A8: the oracle quantises the rows)."""
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    E, Mtot = len(counts), int(off[-1])
+    xb = activations_bf16(seed, Mtot, K, 0.01, 20.0)
+    wq = [quantised_weights(r9q, seed, N, K, tensor=10 + e, check_oracle=False) for e in range(E)]
+    W = torch.stack([q for q, _ in wq])
+    WS = torch.stack([s for _, s in wq])
+    y = r9q.r9q_grouped_gemm_fp8(bf16_to_dev(xb), off.tolist(), W, WS, flags=flags)
+    torch.cuda.synchronize()
+    yb = bits_of(y)
+    for e in range(E):
+        r = slice(int(off[e]), int(off[e + 1]))
+        if off[e + 1] == off[e]:
+            continue
+        we, se = wq[e][0].cpu().numpy(), wq[e][1].cpu().numpy()
+        if flags & r9q.R9Q_GROUPED_WEIGHT_ONLY:
+            acc, gu = oracle.gemm_w8bf16(xb[r], we, se)
+        else:
+            oq, os_ = oracle.quant_group(xb[r])
+            acc, gu = oracle.gemm_w8a8(oq, os_, we, se)
+        if flags & r9q.R9Q_GROUPED_SWIGLU:
+            assert_close(yb[r], f32_of_bits(oracle.swiglu_interleaved(gu)), f"expert {e} h")
+        else:
+            assert_close(yb[r], acc, f"expert {e} y")
+    return y
+
+
+@pytest.mark.parametrize("flags", [0, 1])           # W8A8 with fused quant; weight-only
+@pytest.mark.parametrize("counts", [[3, 0, 1, 16, 5], [70, 3], [0, 0, 2]])
+def test_grouped_gemm(r9q, flags, counts):
+    _grouped_case(r9q, counts, 384, 512, flags, 21)
+
+
+@pytest.mark.parametrize("flags", [2, 3])           # SwiGLU epilogue: W8A8; weight-only
+def test_grouped_gemm_swiglu(r9q, flags):
+    _grouped_case(r9q, [2, 7, 0, 1], 512, 384, flags, 22)
+
+
+def test_grouped_gemm_many_experts(r9q):
+    rng = np.random.default_rng(23)
+    counts = rng.integers(0, 3, 128).tolist()
+    _grouped_case(r9q, counts, 128, 256, 0, 23)
+
+
+def test_grouped_gemm_no_tokens_is_noop(r9q):
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device=dev())
+    w = torch.zeros((2, 128, 256), dtype=torch.uint8, device=dev())
+    ws = torch.ones((2, 1, 2), dtype=torch.float32, device=dev())
+    y = r9q.r9q_grouped_gemm_fp8(x, [0, 0, 0], w, ws)
+    assert y.shape == (0, 128)
+
+
 # ----------------------------------------------------------- expert MLP --
 
 @pytest.mark.parametrize("weight_only", [False, True])

@@ -96,6 +96,28 @@ def test_selftest_rejects_unknown_waits(lib):
     assert f(-1, None) == c["R9Q_ERR_ARG"]
 
 
+def test_grouped_argument_checks(lib):
+    c = _codes()
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    f = lib.r9q_grouped_gemm_fp8
+    f.argtypes = [P, ctypes.POINTER(I64), I64, P, P, P, I64, I64, ctypes.c_int, P]
+    f.restype = ctypes.c_int
+    fake = 1 << 20   # never dereferenced: every case below fails (or returns) before any CUDA call
+
+    def off(*v):
+        return (I64 * len(v))(*v)
+    assert f(fake, off(0, 2, 3), 2, fake, fake, 2 * fake, 128, 128, 4, None) == c["R9Q_ERR_ARG"]   # flags
+    assert f(fake, None, 2, fake, fake, 2 * fake, 128, 128, 0, None) == c["R9Q_ERR_NULL"]
+    assert f(fake, off(0), 0, fake, fake, 2 * fake, 128, 128, 0, None) == c["R9Q_ERR_DIM"]         # E = 0
+    assert f(fake, off(*([0] * 130)), 129, fake, fake, 2 * fake, 128, 128, 0, None) == c["R9Q_ERR_DIM"]
+    assert f(fake, off(1, 2, 3), 2, fake, fake, 2 * fake, 128, 128, 0, None) == c["R9Q_ERR_ARG"]   # offsets[0]
+    assert f(fake, off(0, 3, 2), 2, fake, fake, 2 * fake, 128, 128, 0, None) == c["R9Q_ERR_ARG"]   # decreasing
+    assert f(fake, off(0, 0, 0), 2, None, None, None, 128, 128, 0, None) == c["R9Q_OK"]           # no tokens
+    assert f(fake, off(0, 1, 1), 2, None, fake, 2 * fake, 128, 128, 0, None) == c["R9Q_ERR_NULL"]
+    assert f(fake, off(0, 1, 1), 2, fake, fake, 2 * fake, 100, 128, 0, None) == c["R9Q_ERR_DIM"]
+    assert f(fake, off(0, 1, 1), 2, fake, fake, 2 * fake, 128, 128, 2, None) == c["R9Q_ERR_DIM"]  # SwiGLU N
+
+
 def test_workspace_query(lib):
     c = _codes()
     f = lib.r9q_workspace_bytes
