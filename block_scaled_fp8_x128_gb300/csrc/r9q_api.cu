@@ -155,6 +155,17 @@ void env_plan(int* S, int* G, int* st) {
     *st = v[2];
 }
 
+// Smallest M of the tensor-core W8A8 path; R9Q_TC_MIN_M overrides it (tests and benches only).
+int tc_min_m() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = std::getenv("R9Q_TC_MIN_M");
+        v = s ? std::atoi(s) : kTcMinM;
+        if (v < 1) v = kTcMinM;
+    }
+    return v;
+}
+
 int env_splits() {
     static int v = -1;
     if (v < 0) {
@@ -478,7 +489,7 @@ int r9q_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t N2, int
             if (rc) return rc;
             // decode widths: split-K is reduced in distributed shared memory (no
             // scratch); W8A8 above 64 rows quantises A once into scratch
-            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= kTcMinM && K / 128 <= tc_max_kb()) ? tc_scratch(M, K, true).total : 0;
+            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= tc_min_m() && K / 128 <= tc_max_kb()) ? tc_scratch(M, K, true).total : 0;
             return R9Q_OK;
         }
         case R9Q_OP_GATE_UP_SWIGLU_DOWN: {
@@ -513,7 +524,7 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     if (a_bf16 && aq && (overlaps(aq, (size_t)(M * K), a_bf16, 2 * (size_t)(M * K)) ||
                          overlaps(aq, (size_t)(M * K), w, (size_t)(N * K))))
         return R9Q_ERR_ARG;
-    const bool tc_path = M >= kTcMinM && K / 128 <= tc_max_kb();
+    const bool tc_path = M >= tc_min_m() && K / 128 <= tc_max_kb();
     if (tc_path) {
         // tensor-core path: needs scratch for the ready counters, and for the
         // quantised A unless the caller asked for aq/as as outputs

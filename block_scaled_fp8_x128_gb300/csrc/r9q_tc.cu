@@ -101,22 +101,51 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive TMEM columns of this thread's lane, and the wait for them in
-// the same asm statement, so no use of the registers can be scheduled before
-// the data has arrived.
-__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// 32 consecutive TMEM columns of this thread's lane.  The load is asynchronous:
+// its registers may be used only after a tmem_wait that names them.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
+}
+// Waits for every TMEM load of this thread; the registers of the loads named
+// (r, and s through the empty statement that follows) count as written here,
+// so no use of them moves above the wait.
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[32], uint32_t (&s)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+    asm volatile(""
+                 : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7]),
+                   "+r"(s[8]), "+r"(s[9]), "+r"(s[10]), "+r"(s[11]), "+r"(s[12]), "+r"(s[13]), "+r"(s[14]),
+                   "+r"(s[15]), "+r"(s[16]), "+r"(s[17]), "+r"(s[18]), "+r"(s[19]), "+r"(s[20]), "+r"(s[21]),
+                   "+r"(s[22]), "+r"(s[23]), "+r"(s[24]), "+r"(s[25]), "+r"(s[26]), "+r"(s[27]), "+r"(s[28]),
+                   "+r"(s[29]), "+r"(s[30]), "+r"(s[31])
+                 :
+                 : "memory");
+}
+
+// acc[i] += v[i] * sc for 32 columns, two lanes of packed fp32 FMA at a time
+// (each lane is an IEEE fma, rounded to nearest: the same as fmaf).
+__device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], float sc) {
+    const float2 s2 = make_float2(sc, sc);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; i += 2) {
+        const float2 r = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), s2,
+                                    make_float2(acc[i], acc[i + 1]));
+        acc[i] = r.x;
+        acc[i + 1] = r.y;
+    }
 }
 
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, const void* src) {
@@ -448,20 +477,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*vflags == 0 && !mbar_wait_sleep(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tmem_ld32_wait(taddr + c * 32, v);
-                    if (c == 3) {
-                        // the whole partial is in registers: free the buffer
-                        // for the MMA two k-blocks ahead before the last FMAs
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[ab]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
-                }
+                // Two 32-column loads in flight at a time: the FMAs of one
+                // pair overlap the TMEM latency of the next.
+                uint32_t ra[32], rb[32];
+                tmem_ld32(taddr, ra);
+                tmem_ld32(taddr + 32, rb);
+                tmem_wait(ra, rb);
+                promote32(acc, ra, sc);
+                tmem_ld32(taddr + 64, ra);
+                promote32(acc + 32, rb, sc);
+                tmem_ld32(taddr + 96, rb);
+                tmem_wait(ra, rb);
+                // the whole partial is in registers: free the buffer for the
+                // MMA two k-blocks ahead before the last FMAs
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[ab]);
+                promote32(acc + 64, ra, sc);
+                promote32(acc + 96, rb, sc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&consumed[sb]);     // scale buffer free for a later tile
@@ -531,15 +564,16 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     p.err = err;
     const size_t smem = tc_smem_bytes();
     // The kernel's register split assumes the compiled launch count.
-    static const int launch_regs = []() {
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params) = tc_gemm_kernel;
+    static const int launch_regs = [kern]() {
         cudaFuncAttributes fa = {};
-        return cudaFuncGetAttributes(&fa, tc_gemm_kernel) == cudaSuccess ? fa.numRegs : -1;
+        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
     }();
     if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(tc_gemm_kernel), smem);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_gemm_kernel, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorLaunchOutOfResources;
     const int total = p.mtiles * p.ntiles;
@@ -556,7 +590,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, amap, bmap, ymap, p);
+    return cudaLaunchKernelEx(&cfg, kern, amap, bmap, ymap, p);
 }
 
 }  // namespace r9q
