@@ -207,7 +207,7 @@ def r9q_gemm_fp8_block_qa(a: torch.Tensor | None, w: torch.Tensor, ws: torch.Ten
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=w.device)
     _expect(y, torch.bfloat16, (M, N), "y")
-    if workspace is None and a is not None:
+    if workspace is None:
         need = r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, M, N, K)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=w.device)

@@ -112,17 +112,45 @@ int tmap_2d(const void* base, CUtensorMapDataType dt, int esize, int64_t rows, i
     return r == CUDA_SUCCESS ? R9Q_OK : R9Q_ERR_LAUNCH;
 }
 
-// Workspace of the tensor-core W8A8 path: [aq M x K][as M x KB fp32][ready m-tiles x int32]
+// R9Q_TC_SPLITK=0 keeps every tensor-core W8A8 call on persistent whole-K tiles
+// (tests and benches only).
+bool env_tc_splitk() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = std::getenv("R9Q_TC_SPLITK");
+        v = (s && std::atoi(s) == 0) ? 0 : 1;
+    }
+    return v != 0;
+}
+
+// Workspace of the tensor-core W8A8 path: [aq M x K][as M x KB fp32]
+// [ready m-tiles x int32][done tiles x int32][split-K partials tiles x S x 128 x 256 fp32]
+// (aq/as only when the caller does not take them; done and the partials only
+// with split-K).  The counters are contiguous and zeroed before every launch.
 struct TcScratch {
-    size_t aq, as, ready, total;
+    size_t aq, as, ready, done, counters_end, part, total;
 };
-TcScratch tc_scratch(int64_t M, int64_t K, bool need_aq) {
+TcScratch tc_scratch(int64_t M, int64_t N, int64_t K, bool need_aq, int splits) {
     TcScratch t;
+    const size_t mtiles = (size_t)((M + 127) / 128), tiles = mtiles * (size_t)((N + 255) / 256);
     t.aq = 0;
     t.as = need_aq ? align256((size_t)(M * K)) : 0;
     t.ready = t.as + (need_aq ? align256((size_t)M * (K / 128) * 4) : 0);
-    t.total = t.ready + align256((size_t)((M + 127) / 128) * 4);
+    t.done = t.ready + mtiles * 4;
+    t.counters_end = t.done + (splits > 1 ? tiles * 4 : 0);
+    t.part = align256(t.counters_end);
+    t.total = t.part + (splits > 1 ? tiles * (size_t)splits * 128 * 256 * 4 : 0);
     return t;
+}
+
+// Split-K ranks the tensor-core path uses for (M, N, K) on the current device
+// (R9Q_TC_SPLITK=0: always 1).  Without a device the SM count of a GB300 is
+// assumed, which only matters for workspace queries made without a GPU.
+int tc_splits_for(int64_t M, int64_t N, int64_t K) {
+    int sms = 152;
+    DeviceInfo* d = nullptr;
+    if (current_device(&d) == R9Q_OK) sms = d->sms;
+    return env_tc_splitk() ? tc_plan_splits(M, N, K, sms) : 1;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -489,7 +517,9 @@ int r9q_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t N2, int
             if (rc) return rc;
             // decode widths: split-K is reduced in distributed shared memory (no
             // scratch); W8A8 above 64 rows quantises A once into scratch
-            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= tc_min_m() && K / 128 <= tc_max_kb()) ? tc_scratch(M, K, true).total : 0;
+            *bytes = (op == R9Q_OP_GEMM_W8A8 && M >= tc_min_m() && K / 128 <= tc_max_kb())
+                         ? tc_scratch(M, N, K, true, tc_splits_for(M, N, K)).total
+                         : 0;
             return R9Q_OK;
         }
         case R9Q_OP_GATE_UP_SWIGLU_DOWN: {
@@ -524,40 +554,47 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     if (a_bf16 && aq && (overlaps(aq, (size_t)(M * K), a_bf16, 2 * (size_t)(M * K)) ||
                          overlaps(aq, (size_t)(M * K), w, (size_t)(N * K))))
         return R9Q_ERR_ARG;
+    DeviceInfo* d = nullptr;
+    rc = current_device(&d);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool tc_path = M >= tc_min_m() && K / 128 <= tc_max_kb();
+    // a few tiles: split-K over the SMs (tc_plan_splits)
+    const int splits = tc_path ? (env_tc_splitk() ? tc_plan_splits(M, N, K, d->sms) : 1) : 1;
     if (tc_path) {
-        // tensor-core path: needs scratch for the ready counters, and for the
-        // quantised A unless the caller asked for aq/as as outputs
+        // tensor-core path: needs scratch for the ready counters, for the
+        // quantised A unless the caller asked for aq/as as outputs, and for
+        // the split-K partials
         const bool need_aq = a_bf16 && !aq;
-        const TcScratch sc = tc_scratch(M, K, need_aq);
-        const size_t need = a_bf16 ? sc.total : 0;
+        const TcScratch sc = tc_scratch(M, N, K, need_aq, splits);
+        const size_t need = (a_bf16 || splits > 1) ? sc.total : 0;
         if (need > 0 && (!workspace || workspace_bytes < need)) return R9Q_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return R9Q_ERR_ALIGN;
         if (need > 0 && (overlaps(workspace, need, y_bf16, ybytes) || overlaps(workspace, need, a_bf16, 2 * (size_t)(M * K)) ||
                          overlaps(workspace, need, w, (size_t)(N * K))))
             return R9Q_ERR_ARG;
     }
-    DeviceInfo* d = nullptr;
-    rc = current_device(&d);
-    if (rc) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!tc_path)
         return run_stream_gemm(a_bf16 ? A_QUANT : A_PREQ, EPI_STORE, a_bf16, aq, as, w, ws, y_bf16, N, M, N, K, d, st,
                                g_pdl.load() != 0);
 
     const bool need_aq = a_bf16 && !aq;
-    const TcScratch sc = tc_scratch(M, K, need_aq);
+    const TcScratch sc = tc_scratch(M, N, K, need_aq, splits);
     uint8_t* wsp = static_cast<uint8_t*>(workspace);
     uint8_t* aq_buf = need_aq ? wsp + sc.aq : aq;
     float* as_buf = need_aq ? reinterpret_cast<float*>(wsp + sc.as) : as;
     int* ready = a_bf16 ? reinterpret_cast<int*>(wsp + sc.ready) : nullptr;
+    int* done = splits > 1 ? reinterpret_cast<int*>(wsp + sc.done) : nullptr;
+    float* part = splits > 1 ? reinterpret_cast<float*>(wsp + sc.part) : nullptr;
     CUtensorMap amap, bmap, ymap;
     if ((rc = tmap_2d(aq_buf, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K, 128, 128, &amap)) != 0) return rc;
     if ((rc = tmap_2d(w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K, 128, 256, &bmap)) != 0) return rc;
     if ((rc = tmap_2d(y_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, 64, 128, &ymap)) != 0) return rc;
-    if (ready && cudaMemsetAsync(ready, 0, (size_t)((M + 127) / 128) * 4, st) != cudaSuccess) return R9Q_ERR_LAUNCH;
+    if ((ready || done) && cudaMemsetAsync(wsp + sc.ready, 0, sc.counters_end - sc.ready, st) != cudaSuccess)
+        return R9Q_ERR_LAUNCH;
     return to_status(launch_tc_gemm(amap, bmap, ymap, static_cast<const uint16_t*>(a_bf16), aq_buf, as_buf, ws, ready,
-                                    (int)M, (int)N, (int)K, d->err, d->sms, st));
+                                    static_cast<uint16_t*>(y_bf16), splits, part, done, (int)M, (int)N, (int)K,
+                                    d->err, d->sms, st));
 }
 
 int r9q_gemm_fp8w_bf16a(const void* a_bf16, const uint8_t* w, const float* ws, void* y_bf16, int64_t M,

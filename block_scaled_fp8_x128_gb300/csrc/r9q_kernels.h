@@ -78,9 +78,12 @@ cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 constexpr int kTcMinM = 33;
 size_t tc_smem_bytes();
 int tc_max_kb();            // largest K/128 the tensor-core path takes
+// Split-K ranks per 128x256 tile for (M, N, K) on `sms` SMs (1 = persistent tiles).
+int tc_plan_splits(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
-                           const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
-                           int K, int* err, int sms, cudaStream_t st);
+                           const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, uint16_t* y,
+                           int splits, float* part, int* done, int M, int N, int K, int* err, int sms,
+                           cudaStream_t st);
 
 // The current device's error word (kernels record bounded-wait timeouts there).
 int device_error_word(int** out);

@@ -23,6 +23,12 @@
 // global order and counting finished rows per m-tile; the A loads (and the
 // scale reads) of an m-tile wait (bounded) until its rows are all in.  The
 // codes and scales are those of the standalone quant kernel, bit for bit.
+// Split-K mode (few tiles, e.g. M of a few hundred rows): the grid holds S CTAs
+// per tile, each owning a contiguous range of k-blocks; a CTA writes its fp32
+// partial tile to scratch and publishes it on the tile's counter (release);
+// once all S are in (acquire), CTA rank r sums rows [r*128/S, (r+1)*128/S) of
+// the S partials in rank order (deterministic) and stores bf16.  The grid is
+// cooperative, so every CTA a tile waits for is resident.
 // All waits are bounded: a timeout records R9Q_ERR_TIMEOUT, the kernel drains
 // what it issued, frees its TMEM and returns.
 #include "r9q_device.cuh"
@@ -55,6 +61,8 @@ constexpr int kEpiWarp0 = 4;                     // warps 4..11
 constexpr int kLaunchRegs = 168, kRegsWg0 = 56, kRegsEpi = 224;
 static_assert(kRegsWg0 * 128 + kRegsEpi * 256 == kLaunchRegs * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxSplitK = 8;                    // split-K ranks per tile
+constexpr int kRedU = 4;                         // split-K reduction: float4 outputs in flight a thread
 
 struct Params {
     const uint16_t* a;        // bf16 activations [M][K] (fused) or nullptr
@@ -64,6 +72,10 @@ struct Params {
     int* ready;               // [m-tiles] quantised-row counters (fused), zeroed before launch
     int M, N, K, KB, NB;
     int mtiles, ntiles;
+    uint16_t* y;              // bf16 [M][N] (split-K stores; otherwise the TMA map)
+    int splits;               // S > 1: CTA u owns tile u / S, k-blocks of rank u % S (split-K)
+    float* part;              // split-K: fp32 partial tiles [tiles][S][BM][BN]
+    int* done;                // split-K: [tiles] partials published, zeroed before launch
     int* err;
 };
 
@@ -216,7 +228,9 @@ __device__ __forceinline__ bool wait_rows(const int* ready, int need) { return w
 
 using namespace tc;
 
-// 12 warps: each SM sub-partition holds 3 of them, so up to 168 registers a thread
+// 12 warps: each SM sub-partition holds 3 of them, so up to 168 registers a thread.
+// SPLIT: split-K mode (p.splits > 1); otherwise persistent whole-K tiles.
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const __grid_constant__ CUtensorMap ymap, const Params p) {
@@ -240,6 +254,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int total = p.mtiles * p.ntiles;
     const int KB = p.KB;
+    // Work of this CTA: tiles t_first, t_first + t_step, ... and k-blocks
+    // [kb_lo, kb_hi) of each (split-K: one tile, the rank's k-range).
+    const int S = SPLIT ? p.splits : 1;
+    constexpr bool split = SPLIT;
+    const int rank = split ? (int)blockIdx.x % S : 0;
+    const int t_first = split ? (int)blockIdx.x / S : (int)blockIdx.x;
+    const int t_step = split ? total : (int)gridDim.x;
+    const int kb_lo = rank * KB / S, kb_hi = (rank + 1) * KB / S;
+    // fused quant: a row is nch chunks of CH groups; an m-tile is ready when
+    // its rows * nch chunks are published
+    constexpr int CH = 16;
+    const int nch = (KB + CH - 1) / CH;
+    const int64_t nunits = (int64_t)p.M * nch;
     const bool fused = p.a != nullptr;
     const int nsbuf = KB <= kAsDoubleMaxKB ? 2 : 1;             // scale buffers
     volatile int* vflags = flags;
@@ -275,17 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (fused) {
         // ---------------- quant phase: every warp of the grid ----------------
-        // Rows are dealt out in global order (warp w of the grid takes rows
-        // w, w + 12*grid, ...), so m-tiles fill up from the top while the
-        // GEMM roles below start on the first ones.  Each finished row is
-        // published to its m-tile's ready counter.
+        // A row is a sequence of chunks of 16 groups; chunks are dealt out in
+        // global order (warp w of the grid takes chunks w, w + 12*grid, ...),
+        // so m-tiles fill up from the top and a few rows still spread over
+        // many warps.  Each finished chunk is published to its m-tile's ready
+        // counter (an m-tile is complete at rows * chunks-per-row).  A warp
+        // issues its next chunk's loads before quantising the current one.
+        // Lane l holds 16 values of group 4j + (l >> 3) of the chunk.
         const int gw = blockIdx.x * (kThreads / 32) + warp;
         const int GW = gridDim.x * (kThreads / 32);
-        // A warp's rows are a stream of 16-group chunks; the next chunk's
-        // loads are issued before the current chunk is quantised.  Lane l
-        // holds 16 values of group 4j + (l >> 3) of the chunk.
-        constexpr int CH = 16;
-        const int nch = (KB + CH - 1) / CH;
         const int gl = lane >> 3, el = (lane & 7) * 16;
         auto load = [&](uint4 (&v)[CH / 4][2], int64_t row, int c) {
             const uint16_t* src = p.a + row * p.K;
@@ -315,44 +340,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (c == nch - 1) {
-                // the row is done: publish it to its m-tile's ready counter
-                __syncwarp();
-                if (lane == 0) {
-                    fence_proxy_async_global();
-                    red_release_add(p.ready + row / BM, 1);
-                }
+            // the chunk is done: publish it to its m-tile's ready counter
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_global();
+                red_release_add(p.ready + row / BM, 1);
             }
         };
-        auto next = [&](int64_t& row, int& c) {
-            if (++c == nch) {
-                c = 0;
-                row += GW;
+        // the chunk after the next one goes to L2 while this one is quantised
+        auto prefetch = [&](int64_t u) {
+            if (lane == 0 && u < nunits) {
+                const int64_t row = u / nch;
+                const int c = (int)(u - row * nch);
+                const int groups = min(CH, KB - c * CH);
+                bulk_prefetch_l2(p.a + row * p.K + (int64_t)c * CH * BK, (uint32_t)(groups * BK * 2));
             }
         };
         uint4 va[CH / 4][2], vb[CH / 4][2];
-        int64_t row = gw;
-        int c = 0;
-        if (row < p.M) load(va, row, c);
-        while (row < p.M) {
-            // this warp's next row goes to L2 while this one is quantised
-            if (c == 0 && lane == 0 && row + GW < p.M)
-                bulk_prefetch_l2(p.a + (row + GW) * p.K, (uint32_t)(2 * p.K));
-            int64_t row2 = row;
-            int c2 = c;
-            next(row2, c2);
-            if (row2 < p.M) load(vb, row2, c2);
-            quant(va, row, c);
-            row = row2;
-            c = c2;
-            if (row >= p.M) break;
-            if (c == 0 && lane == 0 && row + GW < p.M)
-                bulk_prefetch_l2(p.a + (row + GW) * p.K, (uint32_t)(2 * p.K));
-            next(row2, c2);
-            if (row2 < p.M) load(va, row2, c2);
-            quant(vb, row, c);
-            row = row2;
-            c = c2;
+        int64_t u = gw;
+        if (u < nunits) load(va, u / nch, (int)(u % nch));
+        while (u < nunits) {
+            prefetch(u + 2 * (int64_t)GW);
+            int64_t u2 = u + GW;
+            if (u2 < nunits) load(vb, u2 / nch, (int)(u2 % nch));
+            quant(va, u / nch, (int)(u % nch));
+            u = u2;
+            if (u >= nunits) break;
+            prefetch(u + 2 * (int64_t)GW);
+            u2 = u + GW;
+            if (u2 < nunits) load(va, u2 / nch, (int)(u2 % nch));
+            quant(vb, u / nch, (int)(u % nch));
+            u = u2;
         }
     }
 
@@ -365,17 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- TMA producer ----------------
             if (lane == 0) {
                 int it = 0;
-                for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
+                for (int t = t_first; t < total && *vflags == 0; t += t_step) {
                     const int mt = t / p.ntiles, nt = t % p.ntiles;
                     if (fused) {
-                        const int need = min(BM, p.M - mt * BM);
+                        const int need = min(BM, p.M - mt * BM) * nch;
                         if (!wait_rows(p.ready + mt, need)) {
                             fail();
                             break;
                         }
                         fence_proxy_async_global();     // the TMA reads what generic stores wrote
                     }
-                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                    for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                         const int st = it % kStages;
                         if (it >= kStages && !mbar_wait_sleep(&empty[st], ((uint32_t)(it / kStages) & 1u) ^ 1u)) {
                             fail();
@@ -394,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- MMA issuer ----------------
             if (lane == 0) {
                 int it = 0;
-                for (int t = blockIdx.x; t < total && *vflags == 0; t += gridDim.x) {
-                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int t = t_first; t < total && *vflags == 0; t += t_step) {
+                    for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                         const int st = it % kStages;
                         const int ab = it & 1;
                         if (!mbar_wait_sleep(&full[st], (uint32_t)(it / kStages) & 1u)) {
@@ -427,14 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // itself): once a tile's rows are quantised and its buffer is
             // free, copy its scales into that buffer.
             int j = 1;
-            for (int t = blockIdx.x + gridDim.x; t < total; t += gridDim.x, ++j) {
+            for (int t = t_first + t_step; t < total; t += t_step, ++j) {
                 const int b = j % nsbuf;
                 const int mt = t / p.ntiles, nt = t % p.ntiles;
                 if (j >= nsbuf && *vflags == 0 &&
                     !mbar_wait_sleep(&consumed[b], (uint32_t)(j / nsbuf - 1) & 1u))
                     fail();
                 const int rows = min(BM, p.M - mt * BM);
-                if (fused && *vflags == 0 && !wait_rows(p.ready + mt, rows)) fail();
+                if (fused && *vflags == 0 && !wait_rows(p.ready + mt, rows * nch)) fail();
                 stage_scales(as_s + b * KB * (BM + 1), ws_s + b * 2 * KB, p.as + (int64_t)mt * BM * KB, rows, p.ws,
                              nt * 2, p.NB, KB, (warp - 2) * 32 + lane, 64);
                 __syncwarp();
@@ -451,14 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = (ew & 3) == 0 && lane == 0;
         uint8_t* stg = outst + wg * (128 * 128);
         int it = 0, j = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
+        for (int t = t_first; t < total; t += t_step, ++j) {
             const int mt = t / p.ntiles, nt = t % p.ntiles;
             const int sb = j % nsbuf;
             if (j == 0) {
                 // the first tile's scales: all 256 epilogue threads copy them
                 // (one round of loads), then stand in for the staging warps
                 const int rows = min(BM, p.M - mt * BM);
-                if (fused && *vflags == 0 && !wait_rows(p.ready + mt, rows)) fail();
+                if (fused && *vflags == 0 && !wait_rows(p.ready + mt, rows * nch)) fail();
                 stage_scales(as_s, ws_s, p.as + (int64_t)mt * BM * KB, rows, p.ws, nt * 2, p.NB, KB, ew * 32 + lane,
                              256);
                 named_sync(3, 256);
@@ -471,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                 const int ab = it & 1;
                 const float sc = as_col[kb * (BM + 1)] * ws_wg[kb];
                 if (*vflags == 0 && !mbar_wait_sleep(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
@@ -498,6 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&consumed[sb]);     // scale buffer free for a later tile
+            if (SPLIT) {
+                // ---- split-K: this rank's partial goes to scratch (reduced below) ----
+                // layout [tile][rank][column quad q][row] of float4: a warp's
+                // 32 rows of one quad are 512 contiguous bytes
+                float4* dst = reinterpret_cast<float4*>(p.part) + ((int64_t)(t * S + rank) * (BN / 4) + wg * 32) * BM + rl;
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    __stcg(dst + c * BM, make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]));
+                continue;
+            }
             // ---- bf16 out: two 64-column boxes through the swizzled staging, TMA stores ----
             const int col0 = nt * BN + wg * 128;
 #pragma unroll
@@ -522,6 +550,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (leader) bulk_wait0();
+        if (SPLIT && t_first < total) {
+            // ---- split-K: publish the partial; once all S are in, rank r sums
+            // rows [r*RB, (r+1)*RB) over ranks 0..S-1 in order (threads take
+            // consecutive rows of one column quad: coalesced partial reads) ----
+            const int t = t_first, mt = t / p.ntiles, nt = t % p.ntiles;
+            __threadfence();
+            named_sync(3, 256);
+            const int et = ew * 32 + lane;          // 0..255
+            if (et == 0) {
+                red_release_add(p.done + t, 1);
+                if (*vflags == 0 && !wait_count(p.done + t, S)) fail();
+            }
+            named_sync(3, 256);
+            const int RB = BM / S;                  // rows reduced by this rank
+            const float4* src = reinterpret_cast<const float4*>(p.part) + (int64_t)t * S * (BN / 4) * BM;
+            for (int u0 = 0; u0 < RB * (BN / 4); u0 += kRedU * 256) {
+                float4 v[kRedU][kMaxSplitK];
+#pragma unroll
+                for (int i = 0; i < kRedU; ++i) {
+                    const int u = u0 + i * 256 + et;
+                    if (u < RB * (BN / 4)) {
+                        const int row = rank * RB + u % RB, c4 = u / RB;
+#pragma unroll
+                        for (int r = 0; r < kMaxSplitK; ++r)
+                            if (r < S) v[i][r] = __ldcg(src + ((int64_t)r * (BN / 4) + c4) * BM + row);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kRedU; ++i) {
+                    const int u = u0 + i * 256 + et;
+                    if (u >= RB * (BN / 4)) continue;
+                    const int row = rank * RB + u % RB, c4 = u / RB;
+                    float4 a = v[i][0];
+#pragma unroll
+                    for (int r = 1; r < kMaxSplitK; ++r)
+                        if (r < S) {
+                            a.x = __fadd_rn(a.x, v[i][r].x);
+                            a.y = __fadd_rn(a.y, v[i][r].y);
+                            a.z = __fadd_rn(a.z, v[i][r].z);
+                            a.w = __fadd_rn(a.w, v[i][r].w);
+                        }
+                    const int m = mt * BM + row, n = nt * BN + 4 * c4;
+                    if (m < p.M && n < p.N)
+                        *reinterpret_cast<uint2*>(p.y + (int64_t)m * p.N + n) =
+                            make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+                }
+            }
+        }
     }
 
     // ---------------- teardown ----------------
@@ -545,9 +621,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t tc_smem_bytes() { return 1024 + (size_t)kStages * kTcStageBytes + kOutBytes + kAsBytes + kWsBytes + 256; }
 int tc_max_kb() { return kMaxKB; }
 
+int tc_plan_splits(int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t KB = K / BK;
+    for (int S = kMaxSplitK; S >= 2; S >>= 1)
+        if (tiles * S <= sms && KB >= S) return S;
+    return 1;
+}
+
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
-                           const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, int M, int N,
-                           int K, int* err, int sms, cudaStream_t st) {
+                           const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, uint16_t* y,
+                           int splits, float* part, int* done, int M, int N, int K, int* err, int sms,
+                           cudaStream_t st) {
     Params p;
     p.a = a;
     p.aq = aq;
@@ -561,15 +646,30 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     p.NB = N / 128;
     p.mtiles = (M + BM - 1) / BM;
     p.ntiles = (N + BN - 1) / BN;
+    p.y = y;
+    p.splits = splits;
+    p.part = part;
+    p.done = done;
     p.err = err;
+    if (splits < 1 || splits > kMaxSplitK || (BM % splits) != 0 || p.KB < splits) return cudaErrorInvalidValue;
+    if (splits > 1 && (part == nullptr || done == nullptr || y == nullptr)) return cudaErrorInvalidValue;
     const size_t smem = tc_smem_bytes();
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params) =
+        splits > 1 ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     // The kernel's register split assumes the compiled launch count.
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params) = tc_gemm_kernel;
-    static const int launch_regs = [kern]() {
-        cudaFuncAttributes fa = {};
-        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
-    }();
-    if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    static const int launch_regs[2] = {[]() {
+                                           cudaFuncAttributes fa = {};
+                                           return cudaFuncGetAttributes(&fa, tc_gemm_kernel<false>) == cudaSuccess
+                                                      ? fa.numRegs
+                                                      : -1;
+                                       }(),
+                                       []() {
+                                           cudaFuncAttributes fa = {};
+                                           return cudaFuncGetAttributes(&fa, tc_gemm_kernel<true>) == cudaSuccess
+                                                      ? fa.numRegs
+                                                      : -1;
+                                       }()};
+    if (launch_regs[splits > 1 ? 1 : 0] != kLaunchRegs) return cudaErrorInvalidConfiguration;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -577,7 +677,10 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorLaunchOutOfResources;
     const int total = p.mtiles * p.ntiles;
-    const int grid = total < sms ? total : sms;
+    // split-K: one CTA per (tile, rank), all resident (the ranks of a tile wait
+    // for each other); otherwise persistent CTAs, at most one per SM
+    const int grid = splits > 1 ? total * splits : (total < sms ? total : sms);
+    if (grid > sms * per_sm) return cudaErrorInvalidConfiguration;
     // Every CTA quantises rows other CTAs wait for, so all CTAs must be
     // resident at once: a cooperative launch guarantees it (one CTA per SM).
     cudaLaunchConfig_t cfg = {};
