@@ -332,15 +332,19 @@ def sweep(torch, r9q, stream, hbm, fp8_peak, src):
         X, W, S, Y = _make_inputs(torch, r9q, kind, M, N, K, seed, p, fac, copies, dev)
         torch.cuda.synchronize()
 
-        def fn(i):
-            r9q.r9q_gemm_fp8_block_qa(X[i], W[i], S[i], y=Y[i])
+        # one scratch for the case's calls (they run in stream order); zeroed once
+        wsp = torch.zeros(max(r9q.r9q_workspace_bytes(r9q.R9Q_OP_GEMM_W8A8, M, N, K), 256), dtype=torch.uint8,
+                          device=dev)
+
+        def fn(i, wsp=wsp):
+            r9q.r9q_gemm_fp8_block_qa(X[i], W[i], S[i], y=Y[i], workspace=wsp)
         calls = 2000 if M <= 255 else 20
         us = timeit(fn, copies, calls)
         flops = 2.0 * M * N * K
         res.append({"config": name, "mode": "W8A8 fused quant", "M": M, "N": N, "K": K, "us_per_call": round(us, 3),
                     "GBps": round(bpc / us / 1e3, 1), "frac_hbm": round(bpc / us / 1e3 / hbm, 4),
                     "TFLOPS": round(flops / us / 1e6, 2), "frac_fp8_nominal": round(flops / us / 1e6 / fp8_peak, 4)})
-        del X, W, S, Y
+        del X, W, S, Y, wsp
         torch.cuda.empty_cache()
 
     # c3: fused expert MLP M=8, H=4096, I=1536, H_out=4096

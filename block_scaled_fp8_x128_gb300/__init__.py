@@ -210,7 +210,9 @@ def r9q_gemm_fp8_block_qa(a: torch.Tensor | None, w: torch.Tensor, ws: torch.Ten
     if workspace is None:
         need = r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, M, N, K)
         if need:
-            workspace = torch.empty(need, dtype=torch.uint8, device=w.device)
+            # a fresh workspace starts zeroed (its counter header); pass one
+            # workspace to every call to avoid this allocation and fill
+            workspace = torch.zeros(need, dtype=torch.uint8, device=w.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.r9q_gemm_fp8_block_qa(_ptr(a), _ptr(aq), _ptr(as_), _ptr(w), _ptr(ws), _ptr(y), M, N, K,
                                       _ptr(workspace), wsb, _stream(stream)), "r9q_gemm_fp8_block_qa")

@@ -123,22 +123,37 @@ bool env_tc_splitk() {
     return v != 0;
 }
 
-// Workspace of the tensor-core W8A8 path: [aq M x K][as M x KB fp32]
-// [ready m-tiles x int32][done tiles x int32][split-K partials tiles x S x 128 x 256 fp32]
-// (aq/as only when the caller does not take them; done and the partials only
-// with split-K).  The counters are contiguous and zeroed before every launch.
+// Workspace of the tensor-core W8A8 path.  Counters first, in a fixed
+// 64 KiB header (so that calls of any shape sharing one workspace find them
+// where the previous call left them at zero): [ready m-tiles][done tiles]
+// [exits] int32; then [aq M x K][as M x KB fp32][split-K partials tiles x S x
+// 128 x 256 fp32] (aq/as only when the caller does not take them, partials
+// only with split-K).  Shapes with more counters than the header holds keep
+// them after the header and have them zeroed before every launch.
+constexpr size_t kCounterHeader = 64 * 1024;
 struct TcScratch {
-    size_t aq, as, ready, done, counters_end, part, total;
+    size_t ready, done, exits, counters_end;   // counters
+    bool self_reset;                           // counters in the header, returned to zero by the kernel
+    size_t aq, as, part, total;
 };
 TcScratch tc_scratch(int64_t M, int64_t N, int64_t K, bool need_aq, int splits) {
     TcScratch t;
     const size_t mtiles = (size_t)((M + 127) / 128), tiles = mtiles * (size_t)((N + 255) / 256);
-    t.aq = 0;
-    t.as = need_aq ? align256((size_t)(M * K)) : 0;
-    t.ready = t.as + (need_aq ? align256((size_t)M * (K / 128) * 4) : 0);
+    const size_t ncnt = mtiles + (splits > 1 ? tiles : 0) + 1;
+    t.self_reset = ncnt * 4 <= kCounterHeader;
+    size_t base = kCounterHeader;
+    if (t.self_reset) {
+        t.ready = 0;
+    } else {
+        t.ready = base;
+        base = align256(base + ncnt * 4);
+    }
     t.done = t.ready + mtiles * 4;
-    t.counters_end = t.done + (splits > 1 ? tiles * 4 : 0);
-    t.part = align256(t.counters_end);
+    t.exits = t.done + (splits > 1 ? tiles * 4 : 0);
+    t.counters_end = t.exits + 4;
+    t.aq = base;
+    t.as = t.aq + (need_aq ? align256((size_t)(M * K)) : 0);
+    t.part = t.as + (need_aq ? align256((size_t)M * (K / 128) * 4) : 0);
     t.total = t.part + (splits > 1 ? tiles * (size_t)splits * 128 * 256 * 4 : 0);
     return t;
 }
@@ -586,14 +601,16 @@ int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as, const uint
     int* ready = a_bf16 ? reinterpret_cast<int*>(wsp + sc.ready) : nullptr;
     int* done = splits > 1 ? reinterpret_cast<int*>(wsp + sc.done) : nullptr;
     float* part = splits > 1 ? reinterpret_cast<float*>(wsp + sc.part) : nullptr;
+    int* exits = (ready || done) && sc.self_reset ? reinterpret_cast<int*>(wsp + sc.exits) : nullptr;
     CUtensorMap amap, bmap, ymap;
     if ((rc = tmap_2d(aq_buf, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K, 128, 128, &amap)) != 0) return rc;
     if ((rc = tmap_2d(w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K, 128, 256, &bmap)) != 0) return rc;
     if ((rc = tmap_2d(y_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, 64, 128, &ymap)) != 0) return rc;
-    if ((ready || done) && cudaMemsetAsync(wsp + sc.ready, 0, sc.counters_end - sc.ready, st) != cudaSuccess)
+    if ((ready || done) && !sc.self_reset &&
+        cudaMemsetAsync(wsp + sc.ready, 0, sc.counters_end - sc.ready, st) != cudaSuccess)
         return R9Q_ERR_LAUNCH;
     return to_status(launch_tc_gemm(amap, bmap, ymap, static_cast<const uint16_t*>(a_bf16), aq_buf, as_buf, ws, ready,
-                                    static_cast<uint16_t*>(y_bf16), splits, part, done, (int)M, (int)N, (int)K,
+                                    static_cast<uint16_t*>(y_bf16), splits, part, done, exits, (int)M, (int)N, (int)K,
                                     d->err, d->sms, st));
 }
 

@@ -82,7 +82,7 @@ int tc_max_kb();            // largest K/128 the tensor-core path takes
 int tc_plan_splits(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
                            const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, uint16_t* y,
-                           int splits, float* part, int* done, int M, int N, int K, int* err, int sms,
+                           int splits, float* part, int* done, int* exits, int M, int N, int K, int* err, int sms,
                            cudaStream_t st);
 
 // The current device's error word (kernels record bounded-wait timeouts there).

@@ -69,13 +69,15 @@ struct Params {
     uint8_t* aq;              // e4m3 scratch / input [M][K]
     float* as;                // fp32 scales [M][KB]
     const float* ws;          // [NB][KB]
-    int* ready;               // [m-tiles] quantised-row counters (fused), zeroed before launch
+    int* ready;               // [m-tiles] quantised-chunk counters (fused), zero at launch
     int M, N, K, KB, NB;
     int mtiles, ntiles;
     uint16_t* y;              // bf16 [M][N] (split-K stores; otherwise the TMA map)
     int splits;               // S > 1: CTA u owns tile u / S, k-blocks of rank u % S (split-K)
     float* part;              // split-K: fp32 partial tiles [tiles][S][BM][BN]
-    int* done;                // split-K: [tiles] partials published, zeroed before launch
+    int* done;                // split-K: [tiles] partials published, zero at launch
+    int* exits;               // CTAs finished; the last one returns ready, done and exits to
+                              // zero (nullptr: the host zeroes the counters before each launch)
     int* err;
 };
 
@@ -249,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* staged = bars + 2 * kStages + 4;                   // [2] a tile's scales are in smem
     uint64_t* consumed = bars + 2 * kStages + 6;                 // [2] ... and no longer needed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
-    int* flags = reinterpret_cast<int*>(tmem_slot + 2);          // [0] error, [1] ring issued, [2] mma k-blocks
+    int* flags = reinterpret_cast<int*>(tmem_slot + 2);          // [0] error, [1] ring issued, [2] mma k-blocks,
+                                                                 // [3] last CTA out
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int total = p.mtiles * p.ntiles;
@@ -611,6 +614,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mmas = flags[2];
         for (int i = max(0, mmas - 2); i < mmas; ++i) (void)mbar_wait(&tfull[i & 1], (uint32_t)(i >> 1) & 1u);
     }
+    if (p.exits != nullptr) {
+        // Every counter access of this CTA is behind the barrier above; the
+        // last CTA of the grid to get here returns the counters to zero for
+        // the next call on the same scratch.
+        if (tid == 0) {
+            __threadfence();
+            flags[3] = (atomicAdd(p.exits, 1) == (int)gridDim.x - 1) ? 1 : 0;
+        }
+        __syncthreads();
+        if (flags[3]) {
+            if (p.ready) for (int i = tid; i < p.mtiles; i += kThreads) p.ready[i] = 0;
+            if (SPLIT && p.done) for (int i = tid; i < total; i += kThreads) p.done[i] = 0;
+            if (tid == 0) *p.exits = 0;
+        }
+    }
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
@@ -631,7 +649,7 @@ int tc_plan_splits(int64_t M, int64_t N, int64_t K, int sms) {
 
 cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap,
                            const uint16_t* a, uint8_t* aq, float* as, const float* ws, int* ready, uint16_t* y,
-                           int splits, float* part, int* done, int M, int N, int K, int* err, int sms,
+                           int splits, float* part, int* done, int* exits, int M, int N, int K, int* err, int sms,
                            cudaStream_t st) {
     Params p;
     p.a = a;
@@ -650,6 +668,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, con
     p.splits = splits;
     p.part = part;
     p.done = done;
+    p.exits = exits;
     p.err = err;
     if (splits < 1 || splits > kMaxSplitK || (BM % splits) != 0 || p.KB < splits) return cudaErrorInvalidValue;
     if (splits > 1 && (part == nullptr || done == nullptr || y == nullptr)) return cudaErrorInvalidValue;

@@ -150,7 +150,14 @@ int r9q_quant_weight_block128(const float* w, int64_t N, int64_t K,
  * Unfused mode (a_bf16 == NULL): aq / as are required inputs.
  * w[N][K] e4m3, ws[N/128][K/128] fp32, y_bf16[M][N].
  * workspace: query r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, ...); when it
- *   reports 0 bytes, workspace may be NULL. */
+ *   reports 0 bytes, workspace may be NULL.  From M = 33 on (the tensor-core
+ *   path) the workspace holds the quantised A, the split-K partials of shapes
+ *   with few 128x256 tiles, and a 64 KiB header of counters: zero the whole
+ *   workspace once before its first use (cudaMemset); every call that
+ *   returns R9Q_OK and whose kernel completes leaves the header at zero again,
+ *   so one workspace can serve any sequence of shapes on one stream.  After a
+ *   call that recorded a device error (r9q_last_device_error), zero it again.
+ *   Calls that may run at the same time on the GPU need separate workspaces. */
 int r9q_gemm_fp8_block_qa(const void* a_bf16, uint8_t* aq, float* as,
                           const uint8_t* w, const float* ws, void* y_bf16,
                           int64_t M, int64_t N, int64_t K,

@@ -214,8 +214,9 @@ def test_w8a8_c4_prefill_sampled(r9q):
 
 @pytest.mark.parametrize("M,N,K", [(3, 256, 384), (5, 384, 640), (13, 128, 128), (17, 640, 256),
                                    (33, 256, 1152), (63, 384, 512), (65, 256, 512), (100, 128, 384),
-                                   (130, 384, 5120),     # tensor-core path, 3-stage ring, two scale buffers
-                                   (200, 256, 8192)])    # ... one scale buffer
+                                   (130, 384, 5120),     # tensor-core path (split-K), two scale buffers
+                                   (200, 256, 8192),     # ... one scale buffer
+                                   (1000, 5120, 256)])   # persistent whole-K tiles: 160 tiles, a partial m-tile
 def test_w8a8_ragged(r9q, M, N, K):
     _w8a8_case(r9q, M, N, K, 0.01, 20.0, 11)
 
@@ -407,6 +408,44 @@ def test_graph_replay_alternating_shapes(r9q):
     torch.cuda.synchronize()
     for e, o in zip(eager, outs):
         assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+
+
+def test_tensor_core_calls_share_one_workspace_in_a_graph(r9q):
+    """W8A8 calls on the tensor-core path (split-K and persistent tiles, fused and
+    unfused quant) share one zeroed workspace: each call returns the counter
+    header to zero, so captured calls replayed many times match the eager ones."""
+    N, K = 1024, 2048
+    wq, ws = quantised_weights(r9q, 9, N, K, check_oracle=False)
+    shapes = (64, 300, 2600, 40)          # split-K 8, split-K 8, persistent (84 tiles), split-K 8
+    xs = [bf16_to_dev(activations_bf16(9, M, K, tensor=M)) for M in shapes]
+    need = max(r9q.r9q_workspace_bytes(r9q.R9Q_OP_GEMM_W8A8, M, N, K) for M in shapes)
+    wsp = torch.zeros(need, dtype=torch.uint8, device=dev())
+    eager = [r9q.r9q_gemm_fp8_block_qa(x, wq, ws, workspace=wsp).clone() for x in xs]
+    uq, us = r9q.r9q_quant_group128(xs[1])
+    eager_unfused = r9q.r9q_gemm_fp8_block_qa(None, wq, ws, aq=uq, as_=us, workspace=wsp).clone()
+    assert torch.equal(eager_unfused.view(torch.int16), eager[1].view(torch.int16))
+    outs = [torch.empty_like(e) for e in eager]
+    out_u = torch.empty_like(eager_unfused)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for x, o in zip(xs, outs):
+            r9q.r9q_gemm_fp8_block_qa(x, wq, ws, y=o, workspace=wsp)
+        r9q.r9q_gemm_fp8_block_qa(None, wq, ws, aq=uq, as_=us, y=out_u, workspace=wsp)
+    for _ in range(50):
+        g.replay()
+    torch.cuda.synchronize()
+    assert r9q.r9q_last_device_error() == 0
+    for e, o in zip(eager, outs):
+        assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+    assert torch.equal(eager_unfused.view(torch.int16), out_u.view(torch.int16))
+    assert torch.count_nonzero(wsp[:64 * 1024]) == 0, "counter header not returned to zero"
+    # the first shape against the oracle
+    xb = activations_bf16(9, shapes[0], K, tensor=shapes[0])
+    oq, os_ = oracle.quant_group(xb)
+    acc, _ = oracle.gemm_w8a8(oq, os_, wq.cpu().numpy(), ws.cpu().numpy())
+    assert_close(bits_of(outs[0]), acc, "W8A8 M=64 from a graph replay")
 
 
 def test_device_error_word_clear(r9q):
