@@ -133,6 +133,34 @@ def test_workspace_query(lib):
     assert f(99, 1, 128, 128, 0, 0, ctypes.byref(out)) == c["R9Q_ERR_ARG"]
 
 
+def test_workspace_query_tensor_core_path(lib):
+    """W8A8 from M = 33 on: a 64 KiB counter header, the quantised A and its
+    scales, and, when few 128x256 tiles leave SMs idle, split-K partials
+    (without a GPU the query plans for a GB300's 152 SMs)."""
+    c = _codes()
+    f = lib.r9q_workspace_bytes
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.POINTER(ctypes.c_size_t)]
+    f.restype = ctypes.c_int
+    out = ctypes.c_size_t(0)
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+
+    header = 64 * 1024
+    # M=128 N=K=4096: 16 tiles, split-K 8 (128 CTAs): partials 16 x 8 x 128 x 256 fp32
+    assert f(c["R9Q_OP_GEMM_W8A8"], 128, 4096, 4096, 0, 0, ctypes.byref(out)) == 0
+    assert out.value == header + a256(128 * 4096) + a256(128 * 32 * 4) + 16 * 8 * 128 * 256 * 4
+    # M=255: 32 tiles, split-K 4
+    assert f(c["R9Q_OP_GEMM_W8A8"], 255, 4096, 4096, 0, 0, ctypes.byref(out)) == 0
+    assert out.value == header + a256(255 * 4096) + a256(255 * 32 * 4) + 32 * 4 * 128 * 256 * 4
+    # M=8192: 1024 tiles, persistent whole-K tiles, no partials
+    assert f(c["R9Q_OP_GEMM_W8A8"], 8192, 4096, 4096, 0, 0, ctypes.byref(out)) == 0
+    assert out.value == header + a256(8192 * 4096) + a256(8192 * 32 * 4)
+    # M=32 stays on the decode stream kernel: nothing
+    assert f(c["R9Q_OP_GEMM_W8A8"], 32, 4096, 4096, 0, 0, ctypes.byref(out)) == 0 and out.value == 0
+
+
 def test_cpu_tensor_rejected_by_binding():
     import torch
     import block_scaled_fp8_x128_gb300 as r9q
