@@ -193,7 +193,11 @@ def r9q_gemm_fp8_block_qa(a: torch.Tensor | None, w: torch.Tensor, ws: torch.Ten
                           as_: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                           M: int | None = None, stream=None) -> torch.Tensor:
     """W8A8.  a (bf16 [M][K]) given: fused quant, aq/as_ optional outputs.
-    a None: aq (uint8 [M][K]) / as_ (fp32 [M][K/128]) are the inputs."""
+    a None: aq (uint8 [M][K]) / as_ (fp32 [M][K/128]) are the inputs.
+    workspace: uint8 device tensor of at least r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, M, N, K)
+    bytes, zero-filled before its first use (e.g. torch.zeros); the calls keep its counter
+    header at zero, so one workspace serves any sequence of calls on one stream.  When omitted,
+    a zeroed one is allocated for this call."""
     N, K = w.shape
     src = a if a is not None else aq
     if src is None:
