@@ -306,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (fused) {
         // ---------------- quant phase: every warp of the grid ----------------
         // A row is a sequence of chunks of 16 groups; chunks are dealt out in
-        // global order (warp w of the grid takes chunks w, w + 12*grid, ...),
-        // so m-tiles fill up from the top and a few rows still spread over
-        // many warps.  Each finished chunk is published to its m-tile's ready
+        // global order, consecutive chunks to consecutive CTAs (warp w of CTA
+        // c takes chunks c + grid*w, c + grid*(w + 12), ...), so m-tiles fill
+        // up from the top and a few rows still spread over many SMs.  Each finished chunk is published to its m-tile's ready
         // counter (an m-tile is complete at rows * chunks-per-row).  A warp
         // issues its next chunk's loads before quantising the current one.
         // Lane l holds 16 values of group 4j + (l >> 3) of the chunk.
-        const int gw = blockIdx.x * (kThreads / 32) + warp;
+        const int gw = blockIdx.x + gridDim.x * warp;         // first chunk of this warp
         const int GW = gridDim.x * (kThreads / 32);
         const int gl = lane >> 3, el = (lane & 7) * 16;
         auto load = [&](uint4 (&v)[CH / 4][2], int64_t row, int c) {
@@ -619,8 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // last CTA of the grid to get here returns the counters to zero for
         // the next call on the same scratch.
         if (tid == 0) {
-            __threadfence();
-            flags[3] = (atomicAdd(p.exits, 1) == (int)gridDim.x - 1) ? 1 : 0;
+            int prev;
+            asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.exits) : "memory");
+            flags[3] = (prev == (int)gridDim.x - 1) ? 1 : 0;
         }
         __syncthreads();
         if (flags[3]) {
