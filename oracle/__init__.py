@@ -61,6 +61,11 @@ def _load():
         lib.r9o_gemm_w8a8.argtypes = [P, P, P, P, I64, I64, I64, P, I64, P, P]
         lib.r9o_gemm_w8bf16.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P]
         lib.r9o_swiglu_interleaved.argtypes = [P, I64, I64, P]
+        lib.r9o_expf.restype = ctypes.c_float
+        lib.r9o_expf.argtypes = [ctypes.c_float]
+        lib.r9o_expf_array.argtypes = [P, I64, P]
+        lib.r9o_silu_mul.restype = ctypes.c_float
+        lib.r9o_silu_mul.argtypes = [ctypes.c_float, ctypes.c_float]
         lib.r9o_gate_up_swiglu_down.restype = ctypes.c_int
         lib.r9o_gate_up_swiglu_down.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int,
                                                 P, P, P, P, P]
@@ -180,6 +185,20 @@ def gemm_w8bf16(x_bf16, w, ws, rows=None):
     y = np.empty((R, N), dtype=np.uint16)
     _load().r9o_gemm_w8bf16(_ptr(x), _ptr(w), _ptr(ws), M, N, K, rp, R, _ptr(acc), _ptr(y))
     return acc, y
+
+
+def expf(x: np.ndarray) -> np.ndarray:
+    """The oracle's fp32 exponential (Cody-Waite reduction, degree-7 Taylor
+    polynomial; r9q_oracle.c) of every element of x."""
+    x = _c(x, np.float32)
+    y = np.empty(x.shape, dtype=np.float32)
+    _load().r9o_expf_array(_ptr(x), x.size, _ptr(y))
+    return y
+
+
+def silu_mul(g: float, u: float) -> float:
+    """silu(g) * u in fp32 as the oracle's SwiGLU step computes it (before the bf16 rounding)."""
+    return float(np.float32(_load().r9o_silu_mul(float(np.float32(g)), float(np.float32(u)))))
 
 
 def swiglu_interleaved(gu_bf16):

@@ -31,7 +31,11 @@
  *    acc = acc + partial * (as * ws), blocks in increasing order, all fp32 with
  *    no fused multiply-add (built with -ffp-contract=off), then RNE to bf16.
  *  - SwiGLU: g, u are the bf16-rounded gate_up outputs; h = bf16(silu(g) * u)
- *    with silu evaluated in double (libm exp) and one rounding to bf16.
+ *    evaluated in fp32 as a separate SwiGLU pass after a bf16 GEMM would:
+ *    e = exp(-g), d = 1 + e, silu = g / d, h = silu * u, each step one IEEE
+ *    fp32 rounding, then RNE to bf16.  exp is written out below (Cody and
+ *    Waite's reduction, Taylor polynomial) so that its every rounding is
+ *    fixed; the fused path must give the separate pass's bits.
  *
  * Parity pins: tests/test_oracle_pins.py (worked examples, brute force,
  * closed forms, library special cases).
@@ -249,7 +253,60 @@ void r9o_gemm_w8bf16(const uint16_t* x, const uint8_t* w, const float* ws,
     }
 }
 
+/* ------------------------------------------------------------------ exp ---- */
+
+/* e^x in fp32 by the method of W. J. Cody and W. Waite ("Software Manual for
+ * the Elementary Functions", 1980, chapter on EXP): write x = k*ln2 + r with k
+ * the integer nearest to x*log2(e), so |r| <= ln2/2; ln2 is carried as a head
+ * (ln2 rounded to fp32) plus a tail (the fp32 rounding of what the head
+ * misses), and r is formed with one fused multiply-add per part.  e^r is the
+ * Taylor series of the exponential to degree 7, sum_{n<=7} r^n/n!, evaluated
+ * by Horner's rule with fused multiply-adds (the first neglected term,
+ * r^8/8!, is below 1e-8 relative for |r| <= ln2/2).  Finally e^x = e^r * 2^k
+ * with a single rounding (ldexpf).  Arguments beyond the fp32 range are
+ * settled first: above 88.8 the result overflows (+inf), below -104 it is
+ * less than half the smallest subnormal (+0).  Each constant is the fp32
+ * value nearest to the stated real number. */
+static const float kLog2e = 0x1.715476p+0f;    /* 1/ln 2 */
+static const float kLn2Hi = 0x1.62e430p-1f;    /* ln 2 */
+static const float kLn2Lo = -0x1.05c610p-29f;  /* ln 2 - kLn2Hi */
+static const float kInv3f = 0x1.555556p-3f;    /* 1/3! */
+static const float kInv4f = 0x1.555556p-5f;    /* 1/4! */
+static const float kInv5f = 0x1.111112p-7f;    /* 1/5! */
+static const float kInv6f = 0x1.6c16c2p-10f;   /* 1/6! */
+static const float kInv7f = 0x1.a01a02p-13f;   /* 1/7! */
+
+float r9o_expf(float x) {
+    if (x > 88.8f) return INFINITY;
+    if (x < -104.0f) return 0.0f;
+    float k = rintf(x * kLog2e);
+    float r = fmaf(-k, kLn2Hi, x);
+    r = fmaf(-k, kLn2Lo, r);
+    float p = kInv7f;
+    p = fmaf(p, r, kInv6f);
+    p = fmaf(p, r, kInv5f);
+    p = fmaf(p, r, kInv4f);
+    p = fmaf(p, r, kInv3f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return ldexpf(p, (int)k);
+}
+
+void r9o_expf_array(const float* x, int64_t n, float* y) {
+    for (int64_t i = 0; i < n; ++i) y[i] = r9o_expf(x[i]);
+}
+
 /* --------------------------------------------------------------- SwiGLU ---- */
+
+/* silu(g) * u in fp32: e = exp(-g), silu = g / (1 + e), times u; each
+ * operation rounded once (g < -88.8 gives e = +inf and silu = -0). */
+float r9o_silu_mul(float g, float u) {
+    float e = r9o_expf(-g);
+    float d = 1.0f + e;
+    float silu = g / d;
+    return silu * u;
+}
 
 /* h[m][128j + c] = bf16( silu(g) * u ), g = gu[m][256j + c], u = gu[m][256j + 128 + c]:
  * the gate_up output interleaves gate and up per 128 rows (gate first). */
@@ -257,10 +314,9 @@ void r9o_swiglu_interleaved(const uint16_t* gu, int64_t M, int64_t I, uint16_t* 
     for (int64_t m = 0; m < M; ++m)
         for (int64_t j = 0; j < I / R9O_BLOCK; ++j)
             for (int64_t c = 0; c < R9O_BLOCK; ++c) {
-                double g = bf16_bits_to_f32(gu[m * 2 * I + 2 * R9O_BLOCK * j + c]);
-                double u = bf16_bits_to_f32(gu[m * 2 * I + 2 * R9O_BLOCK * j + R9O_BLOCK + c]);
-                double silu = g / (1.0 + exp(-g));
-                h[m * I + R9O_BLOCK * j + c] = r9o_f64_to_bf16(silu * u);
+                float g = bf16_bits_to_f32(gu[m * 2 * I + 2 * R9O_BLOCK * j + c]);
+                float u = bf16_bits_to_f32(gu[m * 2 * I + 2 * R9O_BLOCK * j + R9O_BLOCK + c]);
+                h[m * I + R9O_BLOCK * j + c] = r9o_f32_to_bf16(r9o_silu_mul(g, u));
             }
 }
 
