@@ -36,6 +36,7 @@ _SIGS = {
     "r9q_e4m3_from_f32": ([_P, _I64, _P, _P], ctypes.c_int),
     "r9q_quant_group128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "r9q_quant_weight_block128": ([_P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "r9q_swiglu_interleaved": ([_P, _I64, _I64, _P, _P], ctypes.c_int),
     "r9q_gemm_fp8_block_qa": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "r9q_gemm_fp8w_bf16a": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "r9q_gate_up_swiglu_down": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, ctypes.c_int,
@@ -165,6 +166,18 @@ def r9q_quant_group128(x: torch.Tensor, xq: torch.Tensor | None = None, xs: torc
     _expect(xs, torch.float32, (M, K // 128), "xs")
     _check(_lib.r9q_quant_group128(_ptr(x), M, K, _ptr(xq), _ptr(xs), _stream(stream)), "r9q_quant_group128")
     return xq, xs
+
+
+def r9q_swiglu_interleaved(gu: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gu bf16 [M][2I] (gate/up interleaved per 128 columns) -> h bf16 [M][I]."""
+    M, I2 = gu.shape
+    I = I2 // 2
+    _expect(gu, torch.bfloat16, (M, 2 * I), "gu")
+    if h is None:
+        h = torch.empty((M, I), dtype=torch.bfloat16, device=gu.device)
+    _expect(h, torch.bfloat16, (M, I), "h")
+    _check(_lib.r9q_swiglu_interleaved(_ptr(gu), M, I, _ptr(h), _stream(stream)), "r9q_swiglu_interleaved")
+    return h
 
 
 def r9q_quant_weight_block128(w: torch.Tensor, wq: torch.Tensor | None = None, ws: torch.Tensor | None = None,

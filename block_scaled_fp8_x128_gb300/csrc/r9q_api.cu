@@ -45,6 +45,7 @@ int current_device(DeviceInfo** out) {
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
             d.status = R9Q_ERR_DEVICE;
             return;
         }
@@ -54,6 +55,7 @@ int current_device(DeviceInfo** out) {
         }
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) {
+            (void)cudaGetLastError();   // no pending error is left for the caller
             d.status = R9Q_ERR_LAUNCH;
             return;
         }
@@ -447,6 +449,19 @@ int r9q_quant_group128(const void* x_bf16, int64_t M, int64_t K, uint8_t* xq, fl
     if (rc) return rc;
     return to_status(launch_quant_group128(static_cast<const uint16_t*>(x_bf16), M, K, xq, xs,
                                            static_cast<cudaStream_t>(stream), d->sms));
+}
+
+int r9q_swiglu_interleaved(const void* gu_bf16, int64_t M, int64_t I, void* h_bf16, void* stream) {
+    if (!gu_bf16 || !h_bf16) return R9Q_ERR_NULL;
+    if (M < 1 || I < 128 || I % 128 || M > INT_MAX / 2 || I > INT_MAX / 2) return R9Q_ERR_DIM;
+    if (!aligned(gu_bf16, 16) || !aligned(h_bf16, 16)) return R9Q_ERR_ALIGN;
+    if (overlaps(gu_bf16, 4 * (size_t)(M * I), h_bf16, 2 * (size_t)(M * I))) return R9Q_ERR_ARG;
+    DeviceInfo* d = nullptr;
+    int rc = current_device(&d);
+    if (rc) return rc;
+    return to_status(launch_swiglu_interleaved(static_cast<const uint16_t*>(gu_bf16), M, I,
+                                               static_cast<uint16_t*>(h_bf16), static_cast<cudaStream_t>(stream),
+                                               d->sms));
 }
 
 int r9q_quant_weight_block128(const float* w, int64_t N, int64_t K, uint8_t* wq, float* ws, void* stream) {

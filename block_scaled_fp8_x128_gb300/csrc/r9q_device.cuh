@@ -146,10 +146,42 @@ __device__ __forceinline__ uint4 quant_group128_lane8(const uint4 (&v)[2], float
     return c;
 }
 
-// silu(g) * u in fp32 (g, u already bf16-rounded); the separate-launch SwiGLU
-// kernel and the fused gate_up epilogue both call this, so they agree bit for bit.
+// e^x in fp32 with every rounding fixed, so that the SwiGLU result does not
+// depend on a math library's implementation.  Method of Cody and Waite
+// ("Software Manual for the Elementary Functions", 1980): k = rint(x log2 e);
+// r = x - k ln2 with ln2 as an fp32 head plus an fp32 tail, one fused
+// multiply-add each (the head step is exact); e^r = sum_{n=0..7} r^n / n!
+// by Horner's rule in fused multiply-adds (|r| <= ln2/2); e^x = e^r 2^k.
+// The scaling is two multiplies by 2^(k/2) and 2^(k - k/2): the first is
+// exact, so the pair rounds once, like an exact ldexp.  x > 88.8 gives +inf,
+// x < -104 gives +0 (e^x below half the smallest subnormal).  Under 1 ulp of
+// the exponential over the fp32 range.
+__device__ __forceinline__ float exp_cw(float x) {
+    if (x > 88.8f) return __int_as_float(0x7F800000);
+    if (x < -104.0f) return 0.0f;
+    const float k = rintf(__fmul_rn(x, 0x1.715476p+0f));        // x / ln2
+    float r = __fmaf_rn(-k, 0x1.62e430p-1f, x);                  // ln2 head
+    r = __fmaf_rn(-k, -0x1.05c610p-29f, r);                      // ln2 tail
+    float p = 0x1.a01a02p-13f;                                   // 1/7!
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);                        // 1/6!
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);                         // 1/5!
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);                         // 1/4!
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);                         // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int ki = static_cast<int>(k);                          // -150 .. 128
+    const int k1 = ki >> 1, k2 = ki - k1;                        // each in -75 .. 64
+    const float s1 = __int_as_float((k1 + 127) << 23);
+    const float s2 = __int_as_float((k2 + 127) << 23);
+    return __fmul_rn(__fmul_rn(p, s1), s2);
+}
+
+// silu(g) * u in fp32 (g, u already bf16-rounded): e = exp(-g), g / (1 + e),
+// times u, each step one IEEE rounding.  The separate-launch SwiGLU kernel and
+// the fused gate_up epilogue both call this, so they agree bit for bit.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    const float e = expf(-g);
+    const float e = exp_cw(-g);
     const float sg = __fdiv_rn(g, __fadd_rn(1.0f, e));
     return __fmul_rn(sg, u);
 }

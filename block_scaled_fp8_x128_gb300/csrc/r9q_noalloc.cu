@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "r9q.h"
+#include "r9q_kernels.h"
 
 namespace {
 
@@ -42,6 +43,7 @@ int scratch_address(void** out) {
     std::call_once(s.once, [&s]() {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();   // leave no pending error behind for the caller's next CUDA call
             s.status = R9Q_ERR_LAUNCH;
             return;
         }
@@ -57,11 +59,17 @@ extern "C" int r9q_gate_up_swiglu_down_noalloc(const void* x_bf16, const uint8_t
                                                const uint8_t* w_dn, const float* s_dn, void* y_bf16, int64_t M,
                                                int64_t H, int64_t I, int64_t H_out, uint8_t* hq_out,
                                                float* hs_out, int flags, void* stream) {
+    if (!x_bf16 || !w_gu || !s_gu || !w_dn || !s_dn || !y_bf16) return R9Q_ERR_NULL;
     if (flags & R9Q_MLP_UNFUSED) return R9Q_ERR_ARG;            // the separate-launch chain needs more scratch
     if (M < 1 || I < 1) return R9Q_ERR_DIM;
     if ((size_t)M * (size_t)I * 2 > kNoAllocScratchBytes) return R9Q_ERR_WORKSPACE;   // beyond the fixed scratch
+    // The library's device check (an sm_103 GPU) comes before the scratch
+    // lookup, so another GPU gets R9Q_ERR_DEVICE and no lookup is attempted.
+    int* err_word = nullptr;
+    int rc = r9q::device_error_word(&err_word);
+    if (rc) return rc;
     void* h = nullptr;
-    const int rc = scratch_address(&h);
+    rc = scratch_address(&h);
     if (rc) return rc;
     // The existing fused path with h in the library's scratch: no workspace.
     return r9q_gate_up_swiglu_down(x_bf16, w_gu, s_gu, w_dn, s_dn, y_bf16, M, H, I, H_out, h, hq_out, hs_out, flags,

@@ -20,7 +20,13 @@
  *
  * Conventions for every entry point:
  *  - All data pointers are DEVICE pointers owned by the caller.  The library
- *    never allocates device memory and keeps no pointer after a call returns.
+ *    never allocates device memory and keeps no caller pointer after a call
+ *    returns.  Its own device state is two file-scope device arrays: a 4-byte
+ *    error word (r9q_last_device_error) and the 1 MiB scratch of
+ *    r9q_gate_up_swiglu_down_noalloc.  Their device addresses are looked up
+ *    once per device and cached; after cudaDeviceReset those cached
+ *    addresses are stale, so the library must not be called on that device
+ *    again in the same process.
  *  - Matrices are row-major and contiguous.  bf16 is passed as void* (16-bit
  *    IEEE bfloat16).  e4m3 codes are uint8_t.
  *  - Data pointers (bf16 / e4m3 / outputs) must be 16-byte aligned; fp32
@@ -132,6 +138,22 @@ int r9q_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, void* stream);
  * one fp32 division per element; an all-zero group gives s = 0 and codes 0. */
 int r9q_quant_group128(const void* x_bf16, int64_t M, int64_t K,
                        uint8_t* xq, float* xs, void* stream);
+
+/* The SwiGLU step of the expert MLP as a separate pass (what
+ * r9q_gate_up_swiglu_down runs with R9Q_MLP_UNFUSED, and what its fused
+ * epilogue reproduces bit for bit; releases page, v0.3.3 "What changed": the
+ * fused MoE decode path, silu(gate)*up on the interleaved gate_up output).
+ *   gu_bf16[M][2I]: gate and up interleaved per 128 columns, columns
+ *     [256j, 256j+128) gate block j, [256j+128, 256j+256) up block j;
+ *   h_bf16[M][I]:   h[m][128j+c] = bf16( silu(g) * u ), g = gu[m][256j+c],
+ *     u = gu[m][256j+128+c], evaluated in fp32 as e = exp(-g), g / (1 + e),
+ *     times u, one IEEE rounding per step; exp is the library's own (Cody and
+ *     Waite's reduction with a degree-7 Taylor polynomial, under 1 ulp), so
+ *     the result is the same on every GPU and driver.
+ * I a positive multiple of 128, M >= 1; both pointers 16-byte aligned, h
+ * not overlapping gu.  Errors: R9Q_ERR_NULL, R9Q_ERR_DIM, R9Q_ERR_ALIGN,
+ * R9Q_ERR_ARG (overlap), R9Q_ERR_DEVICE, R9Q_ERR_LAUNCH. */
+int r9q_swiglu_interleaved(const void* gu_bf16, int64_t M, int64_t I, void* h_bf16, void* stream);
 
 /* Weight quantisation with one fp32 scale per 128x128 block (set-up, not the
  * hot path): w[N][K] fp32 -> wq[N][K] e4m3, ws[N/128][K/128] fp32,

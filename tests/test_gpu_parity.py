@@ -208,7 +208,14 @@ def test_w8a8_c4(r9q, M):
 
 
 def test_w8a8_c4_prefill_sampled(r9q):
-    rows = np.array([0, 1, 127, 128, 1000, 4095, 4096, 6001, 8190, 8191])
+    """M = 8192: the full aq/as against the oracle, and the output on one row of
+    every 128-row m-tile (each m-tile is a different (CTA, persistent
+    iteration) of the tensor-core kernel), the row's position in the tile
+    rotating over the four 32-lane quarters of the TMEM accumulator, plus the
+    first and last rows."""
+    t = np.arange(8192 // 128)
+    rows = 128 * t + 32 * (t % 4) + (t * 7) % 32
+    rows = np.unique(np.concatenate([rows, [0, 1, 127, 128, 8190, 8191]]))
     _w8a8_case(r9q, 8192, 4096, 4096, 0.0, 1.0, 4, rows=rows)
 
 
@@ -289,6 +296,13 @@ def _grouped_case(r9q, counts, N, K, flags, seed):
             assert_close(yb[r], f32_of_bits(oracle.swiglu_interleaved(gu)), f"expert {e} h")
         else:
             assert_close(yb[r], acc, f"expert {e} y")
+    if flags & r9q.R9Q_GROUPED_SWIGLU:
+        # the same launch without the epilogue gives the GPU's own bf16 gate/up
+        # values; h must be the oracle's SwiGLU of exactly those, bit for bit
+        gu_gpu = r9q.r9q_grouped_gemm_fp8(bf16_to_dev(xb), off.tolist(), W, WS,
+                                          flags=flags & ~r9q.R9Q_GROUPED_SWIGLU)
+        torch.cuda.synchronize()
+        assert np.array_equal(yb, oracle.swiglu_interleaved(bits_of(gu_gpu))), "h != oracle SwiGLU of the GPU's g, u"
     return y
 
 
@@ -348,9 +362,23 @@ def test_mlp_fused_vs_unfused_and_oracle(r9q, weight_only, M, H, I, Ho):
     hb = bits_of(h0)
     assert_close(hb, f32_of_bits(ref["h"]), "h")
     assert_close(bits_of(y0), f32_of_bits(ref["y"]), "y")
+    # The GPU's own bf16 gate/up values (the gate_up GEMM without its
+    # epilogue: a one-expert grouped launch runs the MLP's stream kernel with
+    # the same plan), within the GEMM bound of the oracle's accumulators ...
+    gu_gpu = bits_of(r9q.r9q_grouped_gemm_fp8(x, [0, M], wgu[None], sgu[None],
+                                              flags=r9q.R9Q_GROUPED_WEIGHT_ONLY if weight_only else 0))
+    if weight_only:
+        gacc, _ = oracle.gemm_w8bf16(xb, wgu.cpu().numpy(), sgu.cpu().numpy())
+    else:
+        xq, xs = oracle.quant_group(xb)
+        gacc, _ = oracle.gemm_w8a8(xq, xs, wgu.cpu().numpy(), sgu.cpu().numpy())
+    assert_close(gu_gpu, gacc, "gate_up")
+    # ... and h is the oracle's fp32 SwiGLU of exactly those values, bit for bit
+    h_ref = oracle.swiglu_interleaved(gu_gpu)
+    assert np.array_equal(hb, h_ref), f"h: {int((hb != h_ref).sum())} elements differ from the oracle SwiGLU"
     if not weight_only:
-        # the row quant of the GPU's own h must match the oracle's quant bit for bit
-        oq, os_ = oracle.quant_group(hb)
+        # the down GEMM's fp8 operand: the oracle's row quant of that h, bit for bit
+        oq, os_ = oracle.quant_group(h_ref)
         assert np.array_equal(hq0.cpu().numpy(), oq) and np.array_equal(hs0.cpu().numpy(), os_)
         # and y against the oracle's down GEMM on those operands
         acc, _ = oracle.gemm_w8a8(oq, os_, wdn.cpu().numpy(), sdn.cpu().numpy())
@@ -358,6 +386,32 @@ def test_mlp_fused_vs_unfused_and_oracle(r9q, weight_only, M, H, I, Ho):
     else:
         acc, _ = oracle.gemm_w8bf16(hb, wdn.cpu().numpy(), sdn.cpu().numpy())
         assert_close(bits_of(y0), acc, "y from the GPU's h")
+
+
+def test_swiglu_every_bf16_gate_bit_exact(r9q):
+    """The SwiGLU pass (the library's own exp, fp32 steps) against the oracle,
+    bit for bit, for every finite bf16 gate value against four up rows:
+    u = 1, u = -3, random normal values and random finite bf16 patterns."""
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    g = b[np.isfinite(f32_of_bits(b))]
+    I = g.size                                     # 65280 = 510 * 128
+    rng = np.random.default_rng(31)
+    u = np.stack([np.full(I, synth.to_bf16_bits(np.float32([1.0]))[0], np.uint16),
+                  np.full(I, synth.to_bf16_bits(np.float32([-3.0]))[0], np.uint16),
+                  synth.to_bf16_bits((rng.standard_normal(I) * 10).astype(np.float32)),
+                  rng.permutation(g)])
+    M = u.shape[0]
+    gu = np.empty((M, 2 * I), np.uint16)
+    v = gu.reshape(M, I // 128, 2, 128)
+    v[:, :, 0, :] = g.reshape(I // 128, 128)[None]
+    v[:, :, 1, :] = u.reshape(M, I // 128, 128)
+    h = r9q.r9q_swiglu_interleaved(bf16_to_dev(gu))
+    torch.cuda.synchronize()
+    ref = oracle.swiglu_interleaved(gu)
+    got = bits_of(h)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, [(hex(int(g[j])), hex(int(u[i, j])), hex(int(got[i, j])), hex(int(ref[i, j])))
+                           for i, j in bad[:5]]
 
 
 def test_mlp_without_optional_outputs(r9q):

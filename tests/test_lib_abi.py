@@ -87,6 +87,31 @@ def test_host_argument_checks(lib):
     assert g(*base, 8, 256, 200, 256, None, None, None, 0, None, 0, None) == c["R9Q_ERR_DIM"]
 
 
+def test_noalloc_and_swiglu_argument_checks(lib):
+    """The allocation-free MLP checks its pointers and flags before it looks at
+    the device or its scratch; the SwiGLU pass checks pointers, sizes,
+    alignment and overlap.  Every case fails before any CUDA call."""
+    c = _codes()
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    fake = 1 << 20
+    f = lib.r9q_gate_up_swiglu_down_noalloc
+    f.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, P, P, ctypes.c_int, P]
+    f.restype = ctypes.c_int
+    base = [fake, 2 * fake, 3 * fake, 4 * fake, 5 * fake, 6 * fake]
+    assert f(None, *base[1:], 8, 256, 256, 256, None, None, 0, None) == c["R9Q_ERR_NULL"]
+    assert f(*base[:5], None, 8, 256, 256, 256, None, None, 0, None) == c["R9Q_ERR_NULL"]
+    assert f(*base, 8, 256, 256, 256, None, None, 2, None) == c["R9Q_ERR_ARG"]          # R9Q_MLP_UNFUSED
+    assert f(*base, 4096, 256, 256, 256, None, None, 0, None) == c["R9Q_ERR_WORKSPACE"]  # M*I > 524288
+    g = lib.r9q_swiglu_interleaved
+    g.argtypes = [P, I64, I64, P, P]
+    g.restype = ctypes.c_int
+    assert g(None, 2, 128, fake, None) == c["R9Q_ERR_NULL"]
+    assert g(fake, 2, 100, 2 * fake, None) == c["R9Q_ERR_DIM"]
+    assert g(fake, 0, 128, 2 * fake, None) == c["R9Q_ERR_DIM"]
+    assert g(fake + 4, 2, 128, 2 * fake, None) == c["R9Q_ERR_ALIGN"]
+    assert g(fake, 2, 128, fake + 256, None) == c["R9Q_ERR_ARG"]                  # h inside gu
+
+
 def test_selftest_rejects_unknown_waits(lib):
     c = _codes()
     f = lib.r9q_selftest_wait_timeout
