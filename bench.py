@@ -13,8 +13,8 @@ stream bracket exactly K steps, with a device synchronise on both sides.  SM
 clocks and throttle reasons are sampled through NVML (read-only) during the
 timed region.  A sweep over the other configurations follows the headline.
 
---impl reference times the CPU oracle (test infrastructure, single thread) on a
-bounded sample of the same workload and prints the same JSON line.
+--impl reference times the CPU oracle (test infrastructure, plain C, single
+thread) on whole calls of the same workload and prints the same JSON line.
 """
 from __future__ import annotations
 
@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
+SPIN_CYCLES = 400_000          # ~0.2 ms at 2 GHz
 FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 
@@ -195,8 +196,9 @@ def _time_steps(torch, fn, K, copies, stream, sampler=None):
     reps, rem = divmod(K, G)
     g_full = _graph(torch, fn, G, copies, stream) if reps else None
     g_rem = _graph(torch, fn, rem, copies, stream) if rem else None
-    if g_full:
-        g_full.replay()        # upload
+    for g in (g_full, g_rem):      # upload and run once: the timed replays are warm
+        if g:
+            g.replay()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -206,6 +208,10 @@ def _time_steps(torch, fn, K, copies, stream, sampler=None):
         torch.cuda.synchronize()
         if _BARRIER:
             _BARRIER()
+        # a short device-side spin ahead of the start event keeps the stream
+        # busy while the host submits the graph launches, so the timed region
+        # holds the K steps' device work and not the host's submission latency
+        torch.cuda._sleep(SPIN_CYCLES)
         e0.record(stream)
         for _ in range(reps):
             g_full.replay()
@@ -219,6 +225,47 @@ def _time_steps(torch, fn, K, copies, stream, sampler=None):
     return e0.elapsed_time(e1), clocks
 
 
+def measure_fp8_peak(torch, stream, sampler=None):
+    """Dense fp8 (e4m3) tensor throughput of the library-free reference point:
+    torch._scaled_mm (cuBLASLt) at 8192^3, bf16 out, unit scales; ten timed
+    batches of ten back-to-back GEMMs, best batch, clocks sampled meanwhile."""
+    n = 8192
+    try:
+        gen = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn((n, n), device="cuda", generator=gen).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device="cuda", generator=gen).to(torch.float8_e4m3fn)
+        one = torch.ones((), device="cuda", dtype=torch.float32)
+        bt = b.t()                                  # column-major operand
+
+        def mm():
+            return torch._scaled_mm(a, bt, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                mm()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+        best = float("inf")
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(SPIN_CYCLES)
+                e0.record(stream)
+                for _ in range(10):
+                    mm()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 10)
+        clocks = sampler.stop() if sampler else None
+        del a, b, bt
+        torch.cuda.empty_cache()
+        return {"tflops": round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1), "ms_per_gemm": round(best, 4),
+                "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3, best of 10 batches of 10", "clocks": clocks}
+    except Exception as e:                     # no fp8 GEMM in this torch build
+        return {"tflops": None, "error": f"{type(e).__name__}: {e}"[:200]}
+
+
 def run_gpu(args):
     import torch
     import block_scaled_fp8_x128_gb300 as r9q
@@ -226,8 +273,9 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     hbm, bf16, src = peaks()
-    fp8_peak = 2.0 * bf16           # nominal fp8:bf16 dense ratio of 2 on the measured bf16 peak
+    fp8_nominal = 2.0 * bf16        # nominal fp8:bf16 dense ratio of 2 on the measured bf16 peak
     stream = torch.cuda.Stream()
+    fp8_meas = measure_fp8_peak(torch, stream, ClockSampler(local)) if not args.no_sweep else None
 
     # ---- headline: weight-only decode GEMM, M=16, N=K=4096, seed 1 ----
     M, N, K_ = 16, 4096, 4096
@@ -272,7 +320,7 @@ def run_gpu(args):
         us_e2e = ms_e2e * 1e3 / args.steps
 
     out = {
-        "metric": "block-fp8 GEMM us/call & achieved HBM GB/s (M=1..16), fp8 TFLOPS (M=8192)",
+        "metric": METRIC,
         "value": round(gbs, 1),
         "unit": "GB/s",
         "n_gpus": 1,
@@ -285,10 +333,11 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "e4m3 weights x bf16 activations, fp32 accumulate",
         "data": "synthetic (seeded splitmix64/Box-Muller: x~N(0,1) bf16, W~N(0,0.02) fp32 -> e4m3 + 128x128 fp32 scales)",
-        "config": {"workload": "weight-only fp8 decode GEMM M=16 N=4096 K=4096 (seed 1)",
-                   "M": M, "N": N, "K": K_, "bytes_per_call": bpc,
-                   "l2": f"rotating {copies} weight/activation copies ({copies * bpc / 1e6:.0f} MB > 129 MB L2)",
-                   "timing": "CUDA-graph replay of exactly K calls, CUDA events on the replay stream",
+        "config": dict(HEADLINE),
+        "timing": {"l2": f"inputs larger than L2: rotating {copies} weight/activation copies "
+                         f"({copies * bpc / 1e6:.0f} MB > 129 MB L2)",
+                   "how": "CUDA-graph replay of exactly K calls (graphs uploaded and run once before), "
+                          "CUDA events on the replay stream behind a device-side spin",
                    "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4),
@@ -305,13 +354,14 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     if not args.no_sweep:
-        out["sweep"] = sweep(torch, r9q, stream, hbm, fp8_peak, src)
+        out["fp8_peak_measured"] = fp8_meas
+        out["sweep"] = sweep(torch, r9q, stream, hbm, fp8_nominal, (fp8_meas or {}).get("tflops"), src)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     return out
 
 
-def sweep(torch, r9q, stream, hbm, fp8_peak, src):
+def sweep(torch, r9q, stream, hbm, fp8_nominal, fp8_measured, src):
     res = []
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -341,9 +391,13 @@ def sweep(torch, r9q, stream, hbm, fp8_peak, src):
         calls = 2000 if M <= 255 else 20
         us = timeit(fn, copies, calls)
         flops = 2.0 * M * N * K
-        res.append({"config": name, "mode": "W8A8 fused quant", "M": M, "N": N, "K": K, "us_per_call": round(us, 3),
-                    "GBps": round(bpc / us / 1e3, 1), "frac_hbm": round(bpc / us / 1e3 / hbm, 4),
-                    "TFLOPS": round(flops / us / 1e6, 2), "frac_fp8_nominal": round(flops / us / 1e6 / fp8_peak, 4)})
+        row = {"config": name, "mode": "W8A8 fused quant", "M": M, "N": N, "K": K, "us_per_call": round(us, 3),
+               "GBps": round(bpc / us / 1e3, 1), "frac_hbm": round(bpc / us / 1e3 / hbm, 4),
+               "TFLOPS": round(flops / us / 1e6, 2),
+               "frac_fp8_2x_bf16": round(flops / us / 1e6 / fp8_nominal, 4)}
+        if fp8_measured:
+            row["frac_fp8_measured"] = round(flops / us / 1e6 / fp8_measured, 4)
+        res.append(row)
         del X, W, S, Y, wsp
         torch.cuda.empty_cache()
 
@@ -408,52 +462,123 @@ def sweep(torch, r9q, stream, hbm, fp8_peak, src):
 
 # ---------------------------------------------------------- CPU baseline --
 
-def cpu_baseline(budget_s=10.0, steps=None):
-    """The oracle as it stands (single-threaded C, -O2) on the headline workload:
-    whole M=16 x N=4096 x K=4096 weight-only calls, repeated until the budget."""
-    import oracle
-    import synth
-    M, N, K = 16, 4096, 4096
-    xb = synth.to_bf16_bits(synth.activations(1, M, K))
-    wq, ws = oracle.quant_block128(synth.weights(1, N, K))
+HEADLINE = {"workload": "weight-only fp8 decode GEMM M=16 N=4096 K=4096 (seed 1)",
+            "M": 16, "N": 4096, "K": 4096, "bytes_per_call": gemm_bytes(16, 4096, 4096)}
+METRIC = "block-fp8 GEMM us/call & achieved HBM GB/s (M=1..16), fp8 TFLOPS (M=8192)"
+
+
+def _oracle_call(oracle, synth, case, rows):
+    """Build the inputs of one configuration and return a function that runs
+    the oracle on the token rows `rows` of it (W8A8: quant + GEMM)."""
+    name, kind, M, N, K, seed, p, fac = case
+    xb = synth.to_bf16_bits(synth.activations(seed, M, K, p, fac))
+    if kind == "mlp":
+        I, Ho = N, K
+        H = 4096
+        xb = synth.to_bf16_bits(synth.activations(seed, M, H))
+        wgu, sgu = oracle.quant_block128(synth.weights(seed, 2 * I, H, tensor=1))
+        wdn, sdn = oracle.quant_block128(synth.weights(seed, Ho, I, tensor=2))
+        return lambda: oracle.gate_up_swiglu_down(xb[rows], wgu, sgu, wdn, sdn)
+    wq, ws = oracle.quant_block128(synth.weights(seed, N, K))
+    if kind == "w8bf16":
+        return lambda: oracle.gemm_w8bf16(xb, wq, ws, rows=rows)
+
+    def w8a8():
+        q, sc = oracle.quant_group(xb[rows])
+        return oracle.gemm_w8a8(q, sc, wq, ws)
+    return w8a8
+
+
+# (name, kind, M, N, K, seed, outlier p, factor); the MLP row reads N = I, K = H_out
+CPU_CASES = [("c0 W8A8 M=1 N=512 K=1024", "w8a8", 1, 512, 1024, 0, 0.01, 20.0),
+             ("c1 weight-only M=16 N=4096 K=4096", "w8bf16", 16, 4096, 4096, 1, 0.0, 1.0),
+             ("c2 W8A8 M=16 N=12288 K=4096", "w8a8", 16, 12288, 4096, 2, 0.005, 50.0),
+             ("c3 expert MLP M=8 H=4096 I=1536 H_out=4096", "mlp", 8, 1536, 4096, 3, 0.0, 1.0),
+             ("c4 W8A8 M=8192 N=4096 K=4096", "w8a8", 8192, 4096, 4096, 4, 0.0, 1.0)]
+
+
+def _time_oracle(fn, budget_s, min_calls=1):
     calls, t0 = 0, time.perf_counter()
     while True:
-        oracle.gemm_w8bf16(xb, wq, ws)
+        fn()
         calls += 1
         el = time.perf_counter() - t0
-        if (steps is not None and calls >= steps) or (steps is None and el >= budget_s):
-            break
-    us = el * 1e6 / calls
-    return {"value": round(gemm_bytes(M, N, K) / us / 1e3, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "us_per_call": round(us, 1),
-            "sample": f"{calls} whole M=16 N=4096 K=4096 weight-only calls of the C oracle, 1 thread"}
+        if calls >= min_calls and el >= budget_s:
+            return el / calls, calls
+
+
+def cpu_baseline(budget_s=10.0):
+    """The oracle (plain C, -O2) timed on the host cores.  Headline value: the
+    single-threaded oracle as it stands on whole calls of the headline
+    workload.  `configs`: every configuration, on a bounded sample of its
+    token rows (scaled to a whole call by M / rows), single-threaded and with
+    the OpenMP build of the same source on all cores."""
+    import oracle
+    import synth
+    case = CPU_CASES[1]
+    run = _oracle_call(oracle, synth, case, np.arange(16))
+    per, calls = _time_oracle(run, budget_s)
+    us = per * 1e6
+    res = {"value": round(HEADLINE["bytes_per_call"] / us / 1e3, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "us_per_call": round(us, 1),
+           "sample": f"{calls} whole M=16 N=4096 K=4096 weight-only calls of the C oracle, 1 thread"}
+    table = []
+    try:
+        nthreads = oracle.use_all_cores(True)
+        oracle.use_all_cores(False)
+    except Exception as e:                  # no OpenMP on this host compiler
+        nthreads = 0
+        table.append({"error": f"OpenMP build unavailable: {e}"[:200]})
+    for case in CPU_CASES:
+        name, kind, M, N, K = case[:5]
+        rows = np.arange(min(M, 16)) if M <= 16 else np.linspace(0, M - 1, 8).astype(np.int64)
+        scale = M / len(rows)
+        entry = {"config": name, "sample_rows": int(len(rows)), "scaled_to_M": M}
+        for label, threads in (("1t", 1), ("all", nthreads)):
+            if threads == 0:
+                continue
+            oracle.use_all_cores(threads > 1)
+            fn = _oracle_call(oracle, synth, case, rows)
+            per, calls = _time_oracle(fn, budget_s / 8)
+            us = per * 1e6 * scale
+            entry[f"us_per_call_{label}"] = round(us, 1)
+            entry[f"threads_{label}"] = threads
+            if kind == "mlp":
+                bpc = mlp_bytes(M, 4096, N, K)
+            else:
+                bpc = gemm_bytes(M, N, K)
+            entry[f"GBps_{label}"] = round(bpc / us / 1e3, 4)
+            if kind != "mlp":
+                entry[f"GFLOPS_{label}"] = round(2.0 * M * N * K / us / 1e3, 3)
+        oracle.use_all_cores(False)
+        table.append(entry)
+    res["configs"] = table
+    res["host_cores"] = os.cpu_count()
+    return res
 
 
 def run_reference(args):
-    """The oracle on the host cores, on bounded per-step samples of the headline
-    workload: each step = one token row x all 4096 outputs x K=4096."""
+    """The oracle as it stands (single-threaded C) on the host cores, on the
+    headline workload: each step is one whole M=16 N=4096 K=4096 weight-only
+    call, the same configuration as the GPU arm."""
     import oracle
     import synth
-    M, N, K = 16, 4096, 4096
-    xb = synth.to_bf16_bits(synth.activations(1, M, K))
-    wq, ws = oracle.quant_block128(synth.weights(1, N, K))
-    rows_per_step = 1
-    for i in range(args.warmup):
-        oracle.gemm_w8bf16(xb, wq, ws, rows=np.array([i % M]))
+    run = _oracle_call(oracle, synth, CPU_CASES[1], np.arange(16))
+    for _ in range(args.warmup):
+        run()
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        oracle.gemm_w8bf16(xb, wq, ws, rows=np.array([i % M]))
+    for _ in range(args.steps):
+        run()
     el = time.perf_counter() - t0
-    # a full call is M rows; scale the per-row time to a call
-    us_call = el * 1e6 / args.steps * (M / rows_per_step)
-    gbs = gemm_bytes(M, N, K) / us_call / 1e3
-    return {"impl": "reference", "metric": "block-fp8 GEMM us/call & achieved HBM GB/s (M=1..16), fp8 TFLOPS (M=8192)",
+    us_call = el * 1e6 / args.steps
+    gbs = HEADLINE["bytes_per_call"] / us_call / 1e3
+    return {"impl": "reference", "metric": METRIC,
             "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
-            "config": {"workload": "weight-only fp8 decode GEMM M=16 N=4096 K=4096 (seed 1)"},
+            "config": dict(HEADLINE),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} steps of one token row x 4096 outputs x K=4096"},
+                             "sample": f"{args.steps} whole calls of the headline workload, plain C oracle, 1 thread"},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -520,7 +645,7 @@ def aggregate_over_ranks(out, world, all_reduce_max):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 20000; 20 for --impl reference)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="r9q", choices=["r9q", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
@@ -532,6 +657,8 @@ def main():
                     help="only run a few calls of one workload (for an external profiler) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 20000
     if args.profile_case:
         profile_case(args.profile_case, args.steps)
         return

@@ -142,7 +142,28 @@ def r9q_set_pdl(enable: bool) -> bool:
 
 
 def r9q_last_device_error(stream=None) -> int:
-    return int(_lib.r9q_last_device_error(_stream(stream)))
+    rc = int(_lib.r9q_last_device_error(_stream(stream)))
+    if rc != 0:
+        # a kernel gave up mid-call: its workspace counters may be left non-zero
+        _WORKSPACES.clear()
+    return rc
+
+
+# One zero-filled W8A8 workspace per (device, stream) for calls that pass
+# none.  Every call that completes leaves the workspace's counter header at
+# zero again, so the same tensor serves every later call on that stream
+# (calls on one stream are ordered); it grows when a larger call needs more.
+_WORKSPACES: dict = {}
+
+
+def _stream_workspace(need: int, device: torch.device, stream=None) -> torch.Tensor:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device.index, s.cuda_stream)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = ws
+    return ws
 
 
 def r9q_e4m3_from_f32(x: torch.Tensor, q: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -210,7 +231,9 @@ def r9q_gemm_fp8_block_qa(a: torch.Tensor | None, w: torch.Tensor, ws: torch.Ten
     workspace: uint8 device tensor of at least r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, M, N, K)
     bytes, zero-filled before its first use (e.g. torch.zeros); the calls keep its counter
     header at zero, so one workspace serves any sequence of calls on one stream.  When omitted,
-    a zeroed one is allocated for this call."""
+    the binding reuses one zeroed workspace per (device, stream), allocated (and zero-filled)
+    on the first call that needs it or needs more; pass your own to control that allocation,
+    e.g. before capturing a CUDA graph."""
     N, K = w.shape
     src = a if a is not None else aq
     if src is None:
@@ -227,9 +250,7 @@ def r9q_gemm_fp8_block_qa(a: torch.Tensor | None, w: torch.Tensor, ws: torch.Ten
     if workspace is None:
         need = r9q_workspace_bytes(R9Q_OP_GEMM_W8A8, M, N, K)
         if need:
-            # a fresh workspace starts zeroed (its counter header); pass one
-            # workspace to every call to avoid this allocation and fill
-            workspace = torch.zeros(need, dtype=torch.uint8, device=w.device)
+            workspace = _stream_workspace(need, w.device, stream)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.r9q_gemm_fp8_block_qa(_ptr(a), _ptr(aq), _ptr(as_), _ptr(w), _ptr(ws), _ptr(y), M, N, K,
                                       _ptr(workspace), wsb, _stream(stream)), "r9q_gemm_fp8_block_qa")

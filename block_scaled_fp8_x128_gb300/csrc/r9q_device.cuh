@@ -45,10 +45,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// fl32(a / 448) without a division: y0 = a * RN(1/448), the residual
-// a - 448*y0 is exact in one FMA, and y0 + residual * RN(1/448) rounds to
-// the IEEE quotient.  Checked against IEEE division for every finite bf16 a
-// (the group maxima are bf16 values); tests/test_quant_arith.py.
+// fl32(a / 448) without a division, by Markstein's correction of a quotient
+// with a fused multiply-add (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): y0 = a * RN(1/448), the residual a - 448*y0 is exact in one FMA, and
+// y0 + residual * RN(1/448) rounds to the IEEE quotient.  Checked against IEEE
+// division for every finite bf16 a (the group maxima are bf16 values);
+// tests/test_quant_arith.py.
 __device__ __forceinline__ float div448(float a) {
     const float c = __uint_as_float(0x3B124925u);     // RN(1/448)
     const float y0 = __fmul_rn(a, c);
@@ -57,8 +60,9 @@ __device__ __forceinline__ float div448(float a) {
 }
 
 // fl32(x / s) without a division, for bf16 x and a scale s = fl32(amax/448)
-// of a bf16 amax: with r = RN(1/s), y = RN(x*r), e = RN(x - s*y) (one FMA)
-// and RN(y + e*r) (one FMA) is the IEEE quotient.  Rounding commutes with
+// of a bf16 amax, again by Markstein's FMA correction: with r = RN(1/s),
+// y = RN(x*r), e = RN(x - s*y) (one FMA) and RN(y + e*r) (one FMA) is the
+// IEEE quotient.  Rounding commutes with
 // scaling by powers of two, so only the significands of x and amax matter:
 // tests/test_quant_arith.py runs all 128 x 128 pairs in exact arithmetic.
 // The reduction to significands needs no underflow in e, which holds for

@@ -1,8 +1,11 @@
 // Decode-width block-scaled fp8 GEMM ("stream" kernel), sm_103a.
 //
-// At M <= 64 tokens the GEMM is a weight stream: every weight byte is used by
-// at most 64 tokens, so HBM bandwidth bounds it (r9700-stack v0.3.1 notes: the
-// decode GEMMs' weights are the step's largest stream, and fp8 halves it).
+// At decode widths the GEMM is a weight stream: every weight byte is used by a
+// few tokens, so HBM bandwidth bounds it (r9700-stack v0.3.1 notes: the decode
+// GEMMs' weights are the step's largest stream, and fp8 halves it).  This
+// kernel serves W8A8 calls with M <= 32 (larger W8A8 calls go to the tcgen05
+// kernel), and every weight-only and expert-MLP call, in token chunks of up
+// to 64 rows.
 // Design:
 //  * grid (S, G, ceil(M/MT)) launched as clusters of S CTAs along K.  Cluster
 //    g owns the 128-row weight tiles t = g, g+G, g+2G, ... (one scale block

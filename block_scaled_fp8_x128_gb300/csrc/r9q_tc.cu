@@ -1,5 +1,6 @@
 // Prefill-width block-scaled fp8 GEMM on the 5th-generation tensor cores
-// (tcgen05 + TMEM), sm_103a.  W8A8 only; used for M > 64.
+// (tcgen05 + TMEM), sm_103a.  W8A8 only; r9q_gemm_fp8_block_qa sends every
+// call with M >= 33 here (split-K over the grid while the tiles are few).
 //
 // The contraction is dense here (r9700-stack v0.3.0 notes: fp8 GEMMs on the
 // tiled tensor-core kernel at prefill sizes, and the exact block-scaled fp8

@@ -22,27 +22,44 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "r9q_oracle.c")
 _LIB = os.path.join(_HERE, "libr9q_oracle.so")
-_lib = None
+_LIB_OMP = os.path.join(_HERE, "libr9q_oracle_omp.so")
+_libs = {}
+_all_cores = False
 
 BLOCK = 128
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with the host C compiler (no SIMD flags, no fast math)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + ".tmp.%d" % os.getpid()
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile the oracle with the host C compiler (no SIMD flags, no fast
+    math).  openmp=True builds the same source with -fopenmp: the GEMM loops
+    then split their independent output elements over threads (used only to
+    time the oracle on all host cores; the results are identical)."""
+    lib = _LIB_OMP if openmp else _LIB
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_SRC):
+        tmp = lib + ".tmp.%d" % os.getpid()
         cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+               *(["-fopenmp"] if openmp else []), "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB)
-    return _LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def use_all_cores(enable: bool = True, threads: int = 0) -> int:
+    """Switch the GEMM loops to the OpenMP build (all host cores, or `threads`)
+    or back to the single-threaded build; returns the thread count in use."""
+    global _all_cores
+    _all_cores = bool(enable)
+    lib = _load()
+    if enable and threads > 0:
+        lib.r9o_set_threads(int(threads))
+    return int(lib.r9o_threads())
 
 
 def _load():
-    global _lib
-    if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB)
+    key = _all_cores
+    if key not in _libs:
+        path = build(openmp=key)
+        lib = ctypes.CDLL(path)
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         lib.r9o_e4m3_encode.restype = ctypes.c_uint8
@@ -69,8 +86,10 @@ def _load():
         lib.r9o_gate_up_swiglu_down.restype = ctypes.c_int
         lib.r9o_gate_up_swiglu_down.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int,
                                                 P, P, P, P, P]
-        _lib = lib
-    return _lib
+        lib.r9o_set_threads.argtypes = [ctypes.c_int]
+        lib.r9o_threads.restype = ctypes.c_int
+        _libs[key] = lib
+    return _libs[key]
 
 
 def _ptr(a: np.ndarray | None):

@@ -47,6 +47,30 @@
 
 #define R9O_BLOCK 128
 
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads of the GEMM loops.  The plain build is single-threaded; a build
+ * with -fopenmp (the CPU-baseline timing only) splits the independent output
+ * elements over threads.  Each element is computed by the same sequence of
+ * operations either way, so the results are identical. */
+void r9o_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int r9o_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
 /* ---------------------------------------------------------------- bf16 ---- */
 
 static float bf16_bits_to_f32(uint16_t h) {
@@ -212,9 +236,10 @@ void r9o_gemm_w8a8(const uint8_t* aq, const float* as, const uint8_t* w, const f
     ensure_table();
     int64_t KB = K / R9O_BLOCK;
     int64_t cnt = rows ? nrows : M;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < cnt; ++i) {
-        int64_t m = rows ? rows[i] : i;
         for (int64_t n = 0; n < N; ++n) {
+            int64_t m = rows ? rows[i] : i;
             float acc = 0.0f;
             for (int64_t kb = 0; kb < KB; ++kb) {
                 float p = 0.0f;
@@ -237,9 +262,10 @@ void r9o_gemm_w8bf16(const uint16_t* x, const uint8_t* w, const float* ws,
     ensure_table();
     int64_t KB = K / R9O_BLOCK;
     int64_t cnt = rows ? nrows : M;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < cnt; ++i) {
-        int64_t m = rows ? rows[i] : i;
         for (int64_t n = 0; n < N; ++n) {
+            int64_t m = rows ? rows[i] : i;
             float acc = 0.0f;
             for (int64_t kb = 0; kb < KB; ++kb) {
                 float p = 0.0f;

@@ -40,6 +40,31 @@ def test_noalloc_matches_regular_entry_point_two_calls(r9q, weight_only):
     assert r9q.r9q_last_device_error() == 0
 
 
+@pytest.mark.parametrize("weight_only", [False, True])
+def test_noalloc_back_to_back_with_programmatic_launch(r9q, weight_only):
+    """Programmatic dependent launch on: the next call's gate_up kernel may
+    start while the previous call's down GEMM still reads h from the shared
+    scratch, and must not write h before that GEMM has finished.  Four calls
+    with different inputs are queued on one stream without a synchronise in
+    between; each output must equal the regular entry point's, bit for bit."""
+    M, H, I, Ho = 8, 4096, 1536, 4096
+    wgu, sgu = quantised_weights(r9q, 3, 2 * I, H, tensor=1, check_oracle=False)
+    wdn, sdn = quantised_weights(r9q, 3, Ho, I, tensor=2, check_oracle=False)
+    flags = r9q.R9Q_MLP_WEIGHT_ONLY if weight_only else 0
+    xs = [bf16_to_dev(activations_bf16(40 + i, M, H, 0.01, 20.0)) for i in range(4)]
+    refs = [r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn, flags=flags) for x in xs]
+    torch.cuda.synchronize()
+    prev = r9q.r9q_set_pdl(True)
+    try:
+        outs = [r9q.r9q_gate_up_swiglu_down_noalloc(x, wgu, sgu, wdn, sdn, flags=flags) for x in xs]
+        torch.cuda.synchronize()
+    finally:
+        r9q.r9q_set_pdl(prev)
+    for i, (y, ref) in enumerate(zip(outs, refs)):
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), f"call {i}: not bit-identical"
+    assert r9q.r9q_last_device_error() == 0
+
+
 def test_noalloc_rejects_oversized_and_unfused(r9q):
     M, H, I, Ho = 512, 256, 2048, 256           # M * I = 1,048,576 > 524,288
     x = torch.zeros((M, H), dtype=torch.bfloat16, device=dev())
