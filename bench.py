@@ -428,6 +428,44 @@ def sweep(torch, r9q, stream, hbm, fp8_nominal, fp8_measured, src):
     del WG, WD, HB, YB
     torch.cuda.empty_cache()
 
+    # A decode layer's GEMM sequence at M=8 (attention between them is out of
+    # scope): QKV projection N=12288, output projection 4096x4096, then the
+    # fused expert MLP on the projection's output; every layer reads its own
+    # copy of all weights (copies > 3x L2).  Chained: programmatic dependent
+    # launch on; serialised: off.  Both replay CUDA graphs of whole layers.
+    Ml = 8
+    xl = torch.from_numpy(synth.to_bf16_bits(synth.activations(50, Ml, H, 0.01, 20.0)).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    wq_, sq_ = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(51, 3 * H, H)).to(dev))
+    wo_, so_ = r9q.r9q_quant_weight_block128(torch.from_numpy(synth.weights(52, H, H)).to(dev))
+    bpl = gemm_bytes(Ml, 3 * H, H) + gemm_bytes(Ml, H, H) + mlp_bytes(Ml, H, I, H)
+    copies_l = _copies_for(bpl)
+    LW = [(wq_.clone(), wo_.clone(), wgu.clone(), wdn.clone()) for _ in range(copies_l)]
+    qkv_b = torch.empty((Ml, 3 * H), dtype=torch.bfloat16, device=dev)
+    o_b = torch.empty((Ml, H), dtype=torch.bfloat16, device=dev)
+    y_b = torch.empty((Ml, H), dtype=torch.bfloat16, device=dev)
+    mlp_ws = torch.empty(max(r9q.r9q_workspace_bytes(r9q.R9Q_OP_GATE_UP_SWIGLU_DOWN, Ml, I, H, H), 256),
+                         dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def layer(i):
+        a, b, c, d = LW[i]
+        r9q.r9q_gemm_fp8_block_qa(xl, a, sq_, y=qkv_b)
+        r9q.r9q_gemm_fp8_block_qa(xl, b, so_, y=o_b)
+        r9q.r9q_gate_up_swiglu_down(o_b, c, sgu, d, sdn, y=y_b, workspace=mlp_ws)
+    prev = r9q.r9q_set_pdl(True)
+    us_chained = timeit(layer, copies_l, 500)
+    r9q.r9q_set_pdl(False)
+    us_serial = timeit(layer, copies_l, 500)
+    r9q.r9q_set_pdl(prev)
+    res.append({"config": "layer", "mode": "decode layer GEMMs at M=8 (QKV N=12288, O 4096x4096, expert MLP "
+                "I=1536), 4 launches, W8A8 fused quant, CUDA graph", "M": Ml,
+                "us_per_layer_chained_pdl": round(us_chained, 3), "us_per_layer_serialised": round(us_serial, 3),
+                "GBps_chained": round(bpl / us_chained / 1e3, 1), "frac_hbm_chained": round(bpl / us_chained / 1e3 / hbm, 4),
+                "bytes_per_layer": bpl})
+    del LW
+    torch.cuda.empty_cache()
+
     # MoE decode layer: E experts with T tokens each (the c3 expert shape), grouped
     # gate_up (SwiGLU epilogue) + grouped down (fused quant of h): two launches,
     # against E separate fused expert-MLP calls.  Every expert has its own weight

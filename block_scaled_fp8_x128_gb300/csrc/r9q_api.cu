@@ -236,11 +236,11 @@ size_t mlp_workspace(int64_t M, int64_t I, int flags, bool have_h, bool have_hq)
 
 // ------------------------------------------------------------ planning --
 
-size_t stream_smem_bytes(int MT, int amode, int kbs_max, int ntl_max, int stages) {
+size_t stream_smem_bytes(int MT, int amode, int S, int kbs_max, int ntl_max, int stages) {
     const size_t kslice = (size_t)kbs_max * 128;
     const size_t act_ld = (amode == A_QUANT) ? 2 * kslice + 16 : (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16;
     const size_t npbuf = ntl_max > 1 ? 2 : 1;
-    size_t off = (size_t)stages * kStageBytes + kBarBytes + npbuf * (size_t)MT * kPStride * 4 +
+    size_t off = (size_t)stages * kStageBytes + kBarBytes + npbuf * (size_t)S * stream_recv_rows(S) * MT * 4 +
                  4 * ((size_t)ntl_max * 2 * kbs_max + (size_t)MT * kbs_max);
     off = (off + 15) & ~static_cast<size_t>(15);
     return 1024 + off + (size_t)MT * act_ld;
@@ -270,7 +270,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
             if (ntiles % G) continue;
             const int ntl_max = ntiles / G;
             for (int st = kMaxStages; st >= 2; --st) {
-                const size_t smem = stream_smem_bytes(MT, amode, KB / S, ntl_max, st);
+                const size_t smem = stream_smem_bytes(MT, amode, S, KB / S, ntl_max, st);
                 if (smem > kSmemLimit) continue;
                 int per_sm = (int)((228 * 1024) / (smem + 1024));
                 if (per_sm > per_sm_cap) per_sm = per_sm_cap;
@@ -293,7 +293,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
         for (int S = 1; S <= maxS && bS < 0; ++S) {
             if (KB % S) continue;
             for (int st = kMaxStages; st >= 2; --st)
-                if (stream_smem_bytes(MT, amode, KB / S, 1, st) <= kSmemLimit) {
+                if (stream_smem_bytes(MT, amode, S, KB / S, 1, st) <= kSmemLimit) {
                     bS = S;
                     bG = ntiles;
                     bst = st;
@@ -305,7 +305,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
         int fS, fG, fst;
         env_plan(&fS, &fG, &fst);
         if (fS > 0 && fS <= maxS && KB % fS == 0 && fG > 0 && ntiles % fG == 0 && fst >= 2 && fst <= kMaxStages &&
-            stream_smem_bytes(MT, amode, KB / fS, ntiles / fG, fst) <= kSmemLimit) {
+            stream_smem_bytes(MT, amode, fS, KB / fS, ntiles / fG, fst) <= kSmemLimit) {
             bS = fS;
             bG = fG;
             bst = fst;
@@ -318,7 +318,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
     plan->ntiles = ntiles;
     plan->mchunks = mchunks;
     plan->stages = bst;
-    plan->smem = stream_smem_bytes(MT, amode_launch, KB / bS, (ntiles + bG - 1) / bG, bst);
+    plan->smem = stream_smem_bytes(MT, amode_launch, bS, KB / bS, (ntiles + bG - 1) / bG, bst);
     return true;
 }
 

@@ -13,12 +13,23 @@ enum AMode : int { A_QUANT = 0, A_PREQ = 1, A_BF16 = 2 };
 enum Epi : int { EPI_STORE = 0, EPI_SWIGLU = 1 };
 
 constexpr int kMaxStages = 4;                    // weight ring depth (runtime 2..4)
-constexpr int kCWarps = 8;                       // consumer (MMA) warps, 16 weight rows each
+constexpr int kRowGroups = 1;                    // 16-row mma groups a consumer warp holds
+constexpr int kCWarps = 8 / kRowGroups;          // consumer (MMA) warps, 16 * kRowGroups weight rows each
 constexpr int kStreamThreads = (kCWarps + 1) * 32;
 constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m3)
-constexpr int kPStride = 128 + 4;                // fp32 partial row stride (floats)
 constexpr int kBarBytes = 256;                   // mbarriers + flags
 constexpr int kMaxSplits = 8;                    // cluster size limit (portable)
+
+// Split-K exchange of the stream kernel: every rank of a cluster owns a slice
+// of each 128-row tile's outputs and receives every rank's partial of that
+// slice, [S][stream_recv_rows(S)][MT] fp32 per buffer.  Slices are whole pairs
+// of adjacent output columns (so every bf16x2 store is 4-byte aligned): the 64
+// row pairs of a tile (plain store), or its 32 pairs of h columns, each with
+// its gate and up row (SwiGLU epilogue), split as evenly as the integer
+// division q * S / pairs gives.
+constexpr int stream_recv_rows(int S) {
+    return 2 * ((64 + S - 1) / S) > 4 * ((32 + S - 1) / S) ? 2 * ((64 + S - 1) / S) : 4 * ((32 + S - 1) / S);
+}
 
 struct StreamParams {
     const uint16_t* a;   // bf16 activations [M][K]          (A_QUANT, A_BF16)
@@ -52,7 +63,7 @@ struct StreamPlan {
     size_t smem;         // dynamic shared memory bytes
 };
 
-size_t stream_smem_bytes(int MT, int amode, int kbs_max, int ntl_max, int stages);
+size_t stream_smem_bytes(int MT, int amode, int S, int kbs_max, int ntl_max, int stages);
 // Chooses MT and the split count; returns false when no configuration fits.
 bool plan_stream(int64_t M, int64_t N, int64_t K, int amode, int sms, StreamPlan* plan);
 

@@ -14,23 +14,30 @@
 //  * one producer thread streams the CTA's 128x128 e4m3 weight tiles with 2-D
 //    TMA (128-byte swizzle) through a shared-memory ring guarded by full/empty
 //    mbarriers, running ahead across tile boundaries.
-//  * the CTA's activation slice arrives in shared memory with one bulk copy
-//    per token row, issued right after the first weight stages, and serves
-//    every tile of the CTA.  W8A8: each 128-wide group is quantised in place
+//  * the producer thread initialises the ring barriers and issues the weight
+//    stages as its first act, before any block or cluster barrier; the cluster
+//    barrier and the dependency wait (griddepcontrol.wait) come after.  The
+//    CTA's activation slice then arrives in shared memory with one bulk copy
+//    per token row and serves every tile of the CTA.  W8A8: each 128-wide group is quantised in place
 //    once per CTA at the A-load (shuffle amax, fp32-division-exact quotient,
 //    cvt.rn.satfinite.e4m3x2), byte-identical to the standalone quant kernel.
 //    Weight-only: the bf16 rows are the B operand, their pairs swapped in
 //    registers to match the in-register e4m3 -> bf16 conversion.
-//  * eight MMA warps (16 weight rows each) run swap-AB mma.sync (weights are
-//    the 16-row A operand, tokens the 8-column B operand): m16n8k32 e4m3 for
-//    W8A8, m16n8k16 bf16 for weight-only.  Each k-block's fp32 partial is
+//  * eight MMA warps (16 weight rows each; the row-group count kRowGroups
+//    lets a warp hold several 16-row groups that share its activation
+//    fragments, measured slower) run swap-AB mma.sync (weights are the 16-row
+//    A operand, tokens the 8-column B operand): m16n8k32 e4m3 for W8A8,
+//    m16n8k16 bf16 for weight-only.  Each k-block's fp32 partial is
 //    promoted into register accumulators with as[m][kb] * ws[nb][kb] (the
 //    exact block-scaled form: v0.3.0 notes, exact block-scaled fp8 variant).
-//  * split-K is reduced through distributed shared memory: each CTA parks its
-//    tile partial in one of two shared buffers and signals every peer with a
-//    cluster-scope mbarrier arrive; CTA r then sums slice r of the tile over
-//    ranks 0..S-1 in that fixed order (deterministic, no global workspace)
-//    and tells the peers when it has finished reading.
+//  * split-K is reduced through distributed shared memory, pushed: every rank
+//    owns a slice of each tile's output columns (whole column pairs), and each
+//    MMA warp stores its accumulators straight from registers into the owners'
+//    receive buffers with st.async, whose bytes complete on the owner's
+//    mbarrier (no fence or arrive by the pushers); the owner sums its slice
+//    over ranks 0..S-1 in that fixed order (deterministic, no global
+//    workspace).  With several tiles per CTA the receive buffers alternate,
+//    and an owner tells the pushers when a buffer may be refilled.
 //  * the epilogue writes bf16 y, or (SwiGLU) rounds gate and up to bf16 and
 //    writes h = bf16(silu(g) * u).
 // Every mbarrier wait is bounded; a timeout records R9Q_ERR_TIMEOUT in the
@@ -89,6 +96,31 @@ __device__ __forceinline__ void tile_rows(int t, int& r0, int& r1, int& nb0, int
     }
 }
 
+// Split-K slices (see stream_recv_rows): pair q of the tile's output columns
+// belongs to rank q * S / NP (NP = 64 row pairs for the plain store, 32 pairs
+// of h columns for SwiGLU); rank r's first pair is ceil(r * NP / S).
+template <int EPI>
+__device__ __forceinline__ int slice_pairs() { return EPI == EPI_SWIGLU ? 32 : 64; }
+template <int EPI>
+__device__ __forceinline__ int slice_first_pair(int r, int S) {
+    return (r * slice_pairs<EPI>() + S - 1) / S;
+}
+// Owner rank of tile row j (0..127) and the row's index in the owner's receive
+// area: plain store, rows 2*first .. in order; SwiGLU, gate rows (j < 64) of
+// the owner's h columns first, then their up rows (index cap + c, where cap =
+// 2 * ceil(32 / S) columns is the most a slice holds).
+template <int EPI>
+__device__ __forceinline__ void slice_of(int j, int S, int& owner, int& u) {
+    if (EPI == EPI_SWIGLU) {
+        const int c = j & 63;
+        owner = (c >> 1) * S / 32;
+        u = (j >> 6) * (2 * ((32 + S - 1) / S)) + c - 2 * slice_first_pair<EPI>(owner, S);
+    } else {
+        owner = (j >> 1) * S / 64;
+        u = j - 2 * slice_first_pair<EPI>(owner, S);
+    }
+}
+
 // The kernel body for the token rows [m0, m0 + mvalid) (mvalid >= 1) of one
 // problem whose weight rows start at wrow0 and whose block-scale rows start at
 // nbase (both 0 for a single GEMM; an expert's offsets in the grouped launch).
@@ -122,12 +154,13 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     uint64_t* full = bars;                       // [kMaxStages]
     uint64_t* empty = bars + kMaxStages;         // [kMaxStages]
     uint64_t* abar = bars + 2 * kMaxStages;      // activation bulk copies
-    uint64_t* pfull = abar + 1;                  // [2] every rank's partial is parked
-    uint64_t* pfree = abar + 3;                  // [2] every rank has read my partial
+    uint64_t* rfull = abar + 1;                  // [2] every rank's slice of a tile has landed in buffer b
+    uint64_t* rfree = abar + 3;                  // [2] every rank has summed what I pushed into its buffer b
     int* flags = reinterpret_cast<int*>(bars + 2 * kMaxStages + 5);   // [0] error, [1] issued
-    float* P = reinterpret_cast<float*>(smem + nst * kStageBytes + kBarBytes);   // [npbuf][MT][kPStride]
-    const int npbuf = ntl_max > 1 ? 2 : 1;                            // partial buffers
-    float* ws_s = P + npbuf * MT * kPStride;                          // [ntl_max][2][kbs_max]
+    const int rr = stream_recv_rows(S);                               // receive rows per source rank
+    float* R = reinterpret_cast<float*>(smem + nst * kStageBytes + kBarBytes);   // [npbuf][S][rr][MT]
+    const int npbuf = ntl_max > 1 ? 2 : 1;                            // receive buffers
+    float* ws_s = R + npbuf * S * rr * MT;                            // [ntl_max][2][kbs_max]
     float* as_s = ws_s + ntl_max * 2 * kbs_max;                       // [MT][kbs_max]
     uintptr_t act_addr = reinterpret_cast<uintptr_t>(as_s + MT * kbs_max);
     uint8_t* act = reinterpret_cast<uint8_t*>((act_addr + 15) & ~static_cast<uintptr_t>(15));
@@ -138,34 +171,18 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     const int act_ld = (AMODE == A_QUANT) ? (2 * kslice + 16) : (AMODE == A_BF16) ? (2 * kslice + 32) : (kslice + 16);
     const int row_bytes = (AMODE == A_PREQ) ? nkb * kBlock : 2 * nkb * kBlock;   // bytes copied per token
 
-    if (tid == 0) {
+    // ---- producer prologue: its barriers, then the weight ring at once ----
+    const bool producer = (warp == kCWarps && lane == 0);
+    const int npro = min(iters, nst);
+    if (producer) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCWarps);
         }
         mbar_init(abar, 1);
         flags[0] = 0;
-        flags[1] = 0;
+        flags[1] = npro;
         fence_proxy_async_smem();     // the TMA unit sees the initialised ring barriers
-    }
-    if (tid == 32) {
-        mbar_init(&pfull[0], S);
-        mbar_init(&pfull[1], S);
-        mbar_init(&pfree[0], S);
-        mbar_init(&pfree[1], S);
-        fence_mbar_init();            // peers see them once the cluster barrier below completes
-    }
-    // the producer and the MMA warps use the barriers just initialised
-    __syncthreads();
-    // Every peer's barriers must exist before anyone arrives on them remotely:
-    // arrive on the cluster barrier now, wait for it only just before the
-    // first remote arrive, so the weight stream starts at once.
-    cluster_arrive();
-
-    // ---- producer prologue: fill the ring, then fetch the activations ----
-    const bool producer = (warp == kCWarps && lane == 0);
-    const int npro = min(iters, nst);
-    if (producer) {
         tma_prefetch_desc(&wmap);
         for (int it = 0; it < npro; ++it) {
             const int tl = it / nkb, i = it - tl * nkb;
@@ -177,7 +194,6 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             tma_load_2d(ring + it * kStageBytes, &wmap, (kb0 + i) * kBlock, r0, &full[it]);
             tma_load_2d(ring + it * kStageBytes + kStageBytes / 2, &wmap, (kb0 + i) * kBlock, r1, &full[it]);
         }
-        flags[1] = npro;
         // the rest of this CTA's weight slice goes to L2 now, so that the ring
         // refills from L2 and the DRAM stream does not wait for the MMAs
         for (int it = npro; it < iters; ++it) {
@@ -188,6 +204,30 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, wrow0 + r1);
         }
     }
+    // Bytes this rank receives per tile: every rank's values (all MT tokens)
+    // of the rows of my slice (plain store: 2 rows a column pair; SwiGLU: a
+    // gate and an up row per h column).
+    const int q_lo = slice_first_pair<EPI>(split, S), q_hi = slice_first_pair<EPI>(split + 1, S);
+    const uint32_t recv_bytes = (uint32_t)(S * (EPI == EPI_SWIGLU ? 4 : 2) * (q_hi - q_lo) * MT * 4);
+    if (tid == 0) {
+        // rfull: one arrival (mine, with the byte count) plus the peers' bytes
+        mbar_init(&rfull[0], 1);
+        mbar_init(&rfull[1], 1);
+        mbar_init(&rfree[0], S);
+        mbar_init(&rfree[1], S);
+        fence_mbar_init();            // peers see them once the cluster barrier below completes
+        // arm the receive barriers of my first two tiles (peers' bytes may land
+        // before or after; the phase completes when both are in)
+        if (ntl > 0) mbar_expect_tx(&rfull[0], recv_bytes);
+        if (ntl > 1) mbar_expect_tx(&rfull[1], recv_bytes);
+    }
+    // the MMA warps use the barriers just initialised
+    __syncthreads();
+    // Every peer's barriers must exist before anyone arrives on them remotely:
+    // arrive on the cluster barrier now, wait for it only just before the
+    // first remote access.
+    cluster_arrive();
+
     // Weights and their block scales never come from the preceding kernel:
     // load the scales now.  The activation rows may: prefetch them into L2
     // only (no stale data can result) and copy them after the wait.
@@ -206,6 +246,8 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
         ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
         ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
     }
+    // every peer's barriers exist (before any remote access below)
+    cluster_wait();
     pdl_wait();
     if (producer) {
         mbar_expect_tx(abar, (uint32_t)(mvalid * row_bytes));
@@ -264,12 +306,12 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
 
     const int g = lane >> 2, t = lane & 3;
     if (warp < kCWarps) {
-        cluster_wait();
-        // ---- MMA warps: rows [16*warp, 16*warp + 16) of every tile ----
-        const int box = warp >> 2;
+        // ---- MMA warps: rows [16*RG*warp, 16*RG*(warp + 1)) of every tile, as
+        // RG 16-row groups that share every activation fragment the warp loads ----
+        constexpr int RG = kRowGroups;
+        const int box = (warp * 16 * RG) >> 6;           // 64-row half: scale row nb0 or nb1
         const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int lchk = lane >> 4;
-        const int row = warp * 16 + lrow;
         // A failed wait sets flags[0]; from then on every wait is skipped but
         // all MMA warps keep walking the same loop and barrier sequence, so no
         // warp is left waiting at a named barrier.
@@ -278,52 +320,68 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             record_error(p.err, kErrTimeout);
             atomicExch(&flags[0], 1);
         };
-        // Tile tl's partial is parked and announced, then tile tl-1 is reduced:
-        // the wait for the peers' partials of one tile overlaps the MMAs of the next.
+        // Tile tl's partial is pushed, then tile tl-1 is reduced: the wait for
+        // the peers' partials of one tile overlaps the MMAs of the next.
         for (int tl = 0; tl <= ntl; ++tl) {
             if (tl < ntl) {
-                float acc[NT][4];
+                float acc[RG][NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int rg = 0; rg < RG; ++rg)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[rg][nt][e] = 0.0f;
                 const float* wsv_s = ws_s + (tl * 2 + box) * kbs_max;
                 for (int i = 0; i < nkb; ++i) {
                     const int it = tl * nkb + i;
                     const int st = it % nst;
                     if (*vflags == 0 && !mbar_wait(&full[st], (uint32_t)(it / nst) & 1u)) fail();
                     const uint32_t tbase = smem_u32(ring + st * kStageBytes);
-                    float d[NT][4];
+                    float d[RG][NT][4];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
+                    for (int rg = 0; rg < RG; ++rg)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) d[nt][e] = 0.0f;
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) d[rg][nt][e] = 0.0f;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        uint32_t a[4];
                         const int chunk = ks * 2 + lchk;
-                        ldmatrix_x4(tbase + row * 128 + ((chunk ^ (row & 7)) << 4), a[0], a[1], a[2], a[3]);
+                        uint32_t a[RG][4];
+#pragma unroll
+                        for (int rg = 0; rg < RG; ++rg) {
+                            const int row = warp * 16 * RG + rg * 16 + lrow;
+                            ldmatrix_x4(tbase + row * 128 + ((chunk ^ (row & 7)) << 4), a[rg][0], a[rg][1], a[rg][2],
+                                        a[rg][3]);
+                        }
                         if (AMODE != A_BF16) {
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const uint8_t* bp = act + (nt * 8 + g) * act_ld + i * kBlock + ks * 32 + 4 * t;
-                                mma_e4m3_16832(d[nt], a, *reinterpret_cast<const uint32_t*>(bp),
-                                               *reinterpret_cast<const uint32_t*>(bp + 16));
+                                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp);
+                                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 16);
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg) mma_e4m3_16832(d[rg][nt], a[rg], b0, b1);
                             }
                         } else {
-                            uint32_t ev[4], od[4];
+                            uint32_t ev[RG][4], od[RG][4];
 #pragma unroll
-                            for (int r = 0; r < 4; ++r) e4m3x4_to_bf16x2x2(a[r], ev[r], od[r]);
+                            for (int rg = 0; rg < RG; ++rg)
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) e4m3x4_to_bf16x2x2(a[rg][r], ev[rg][r], od[rg][r]);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 const uint8_t* bp = act + (nt * 8 + g) * act_ld + 2 * (i * kBlock + ks * 32 + 4 * t);
                                 // (x0,x1),(x2,x3) -> (x0,x2),(x1,x3): the pairing of e4m3x4_to_bf16x2x2
                                 const uint2 bv = *reinterpret_cast<const uint2*>(bp);
                                 const uint2 cv = *reinterpret_cast<const uint2*>(bp + 32);
-                                mma_bf16_16816(d[nt], ev[0], ev[1], od[0], od[1], __byte_perm(bv.x, bv.y, 0x5410),
-                                               __byte_perm(bv.x, bv.y, 0x7632));
-                                mma_bf16_16816(d[nt], ev[2], ev[3], od[2], od[3], __byte_perm(cv.x, cv.y, 0x5410),
-                                               __byte_perm(cv.x, cv.y, 0x7632));
+                                const uint32_t b0 = __byte_perm(bv.x, bv.y, 0x5410), b1 = __byte_perm(bv.x, bv.y, 0x7632);
+                                const uint32_t c0 = __byte_perm(cv.x, cv.y, 0x5410), c1 = __byte_perm(cv.x, cv.y, 0x7632);
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg) {
+                                    mma_bf16_16816(d[rg][nt], ev[rg][0], ev[rg][1], od[rg][0], od[rg][1], b0, b1);
+                                    mma_bf16_16816(d[rg][nt], ev[rg][2], ev[rg][3], od[rg][2], od[rg][3], c0, c1);
+                                }
                             }
                         }
                     }
@@ -338,115 +396,111 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
                             sc0 = as_s[(nt * 8 + 2 * t) * kbs_max + i] * wsv;
                             sc1 = as_s[(nt * 8 + 2 * t + 1) * kbs_max + i] * wsv;
                         }
-                        acc[nt][0] = fmaf(d[nt][0], sc0, acc[nt][0]);
-                        acc[nt][1] = fmaf(d[nt][1], sc1, acc[nt][1]);
-                        acc[nt][2] = fmaf(d[nt][2], sc0, acc[nt][2]);
-                        acc[nt][3] = fmaf(d[nt][3], sc1, acc[nt][3]);
+#pragma unroll
+                        for (int rg = 0; rg < RG; ++rg) {
+                            acc[rg][nt][0] = fmaf(d[rg][nt][0], sc0, acc[rg][nt][0]);
+                            acc[rg][nt][1] = fmaf(d[rg][nt][1], sc1, acc[rg][nt][1]);
+                            acc[rg][nt][2] = fmaf(d[rg][nt][2], sc0, acc[rg][nt][2]);
+                            acc[rg][nt][3] = fmaf(d[rg][nt][3], sc1, acc[rg][nt][3]);
+                        }
                     }
                 }
 
-                // ---- park the partial in buffer b = tl & 1 (after its last readers are done) ----
+                // ---- push the tile's partial to the ranks that own its rows ----
+                // into buffer b = tl & 1 of each owner, once every owner has
+                // summed what was pushed there two tiles ago; the stores count
+                // their bytes on the owner's rfull[b]
                 const int b = tl & 1;
                 const uint32_t use = (uint32_t)(tl >> 1);
-                if (tl >= 2 && *vflags == 0 && !mbar_wait_cluster(&pfree[b], (use - 1) & 1u)) fail();
-                float* Pb = P + b * MT * kPStride;
+                if (tl >= 2 && *vflags == 0 && !mbar_wait_cluster(&rfree[b], (use - 1) & 1u)) fail();
+                const uint32_t rbase = smem_u32(R + (size_t)b * S * rr * MT) + (uint32_t)(split * rr * MT * 4);
+                const uint32_t rbar = smem_u32(&rfull[b]);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int r = warp * 16 + g;
-                    const int tok = nt * 8 + 2 * t;
-                    Pb[tok * kPStride + r] = acc[nt][0];
-                    Pb[(tok + 1) * kPStride + r] = acc[nt][1];
-                    Pb[tok * kPStride + r + 8] = acc[nt][2];
-                    Pb[(tok + 1) * kPStride + r + 8] = acc[nt][3];
-                }
-                consumer_sync();
-                if (tid == 0) mbar_arrive_all_ranks(&pfull[b], S);
+                for (int rg = 0; rg < RG; ++rg)
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        int owner, u;
+                        slice_of<EPI>(warp * 16 * RG + rg * 16 + g + 8 * h8, S, owner, u);
+                        const uint32_t dst = dsmem_addr(rbase + (uint32_t)(u * MT * 4), (uint32_t)owner);
+                        const uint32_t dbar = dsmem_addr(rbar, (uint32_t)owner);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            st_async_f32x2(dst + (uint32_t)((nt * 8 + 2 * t) * 4), acc[rg][nt][2 * h8],
+                                           acc[rg][nt][2 * h8 + 1], dbar);
+                    }
             }
             if (tl >= 1) {
+                // ---- tile rt: sum my slice over the ranks 0..S-1, in that order ----
                 const int rt = tl - 1;
                 const int tile = group + rt * G;
                 const int b = rt & 1;
                 const uint32_t use = (uint32_t)(rt >> 1);
-                if (*vflags == 0 && !mbar_wait_cluster(&pfull[b], use & 1u)) fail();
-                const float* Pb = P + b * MT * kPStride;
-                // ---- split-K reduction of tile rt, slice `split`, over ranks 0..S-1 + epilogue ----
-                // Sums go to registers first; the peers are told their partials are
-                // free before the global stores, so the release never waits on them.
-                const uint32_t pbase = smem_u32(Pb);
-                constexpr int UPT = (EPI == EPI_SWIGLU) ? 32 : 64;   // units per token
-                constexpr int MAXU = (MT * UPT + kCWarps * 32 - 1) / (kCWarps * 32);   // units per thread, S = 1
-                const int U = MT * UPT;
-                const int u_lo = (split * U) / S, u_hi = ((split + 1) * U) / S;
+                if (*vflags == 0 && !mbar_wait_cluster(&rfull[b], use & 1u)) fail();
+                const float* Rb = R + (size_t)b * S * rr * MT;
+                const int q0 = slice_first_pair<EPI>(split, S), q1 = slice_first_pair<EPI>(split + 1, S);
+                const int units = (q1 - q0) * MT;                   // (column pair, token), token fastest
+                constexpr int MAXU = (64 * MT + kCWarps * 32 - 1) / (kCWarps * 32);   // S = 1 holds the most
+                const int cap = 2 * ((32 + S - 1) / S);              // SwiGLU: up rows follow `cap` gate rows
                 uint32_t outv[MAXU];
 #pragma unroll
-                for (int j = 0; j < MAXU; ++j) {
-                    const int u = u_lo + tid + j * kCWarps * 32;
-                    outv[j] = 0u;
-                    if (u >= u_hi) continue;
-                    const int tok = u / UPT, up = u - tok * UPT;
+                for (int jj = 0; jj < MAXU; ++jj) {
+                    const int q = tid + jj * kCWarps * 32;
+                    outv[jj] = 0u;
+                    if (q >= units) continue;
+                    const int pr = q / MT, tok = q - pr * MT;
                     if (tok >= mvalid) continue;
-                    // all ranks' partials are loaded first (independent remote
-                    // loads in flight together), then summed in rank order
+                    const int u = 2 * pr;
                     if (EPI == EPI_STORE) {
-                        const uint32_t off = (uint32_t)((tok * kPStride + 2 * up) * 4);
-                        float2 v[kMaxSplits];
-#pragma unroll
-                        for (int r = 0; r < kMaxSplits; ++r)
-                            if (r < S) v[r] = ld_dsmem_f32x2(dsmem_addr(pbase + off, (uint32_t)r));
-                        float2 sum = v[0];
-#pragma unroll
-                        for (int r = 1; r < kMaxSplits; ++r)
-                            if (r < S) {
-                                sum.x = __fadd_rn(sum.x, v[r].x);
-                                sum.y = __fadd_rn(sum.y, v[r].y);
-                            }
-                        outv[j] = pack_bf16x2(sum.x, sum.y);
+                        float s0 = Rb[u * MT + tok], s1 = Rb[(u + 1) * MT + tok];
+                        for (int r = 1; r < S; ++r) {
+                            s0 = __fadd_rn(s0, Rb[(r * rr + u) * MT + tok]);
+                            s1 = __fadd_rn(s1, Rb[(r * rr + u + 1) * MT + tok]);
+                        }
+                        outv[jj] = pack_bf16x2(s0, s1);
                     } else {
-                        const uint32_t offg = (uint32_t)((tok * kPStride + 2 * up) * 4);
-                        const uint32_t offu = offg + 64 * 4;
-                        float2 gv[kMaxSplits], uv[kMaxSplits];
-#pragma unroll
-                        for (int r = 0; r < kMaxSplits; ++r)
-                            if (r < S) {
-                                gv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offg, (uint32_t)r));
-                                uv[r] = ld_dsmem_f32x2(dsmem_addr(pbase + offu, (uint32_t)r));
-                            }
-                        float2 gs = gv[0], us = uv[0];
-#pragma unroll
-                        for (int r = 1; r < kMaxSplits; ++r)
-                            if (r < S) {
-                                gs.x = __fadd_rn(gs.x, gv[r].x);
-                                gs.y = __fadd_rn(gs.y, gv[r].y);
-                                us.x = __fadd_rn(us.x, uv[r].x);
-                                us.y = __fadd_rn(us.y, uv[r].y);
-                            }
-                        const float h0 = silu_mul(bf16_round(gs.x), bf16_round(us.x));
-                        const float h1 = silu_mul(bf16_round(gs.y), bf16_round(us.y));
-                        outv[j] = pack_bf16x2(h0, h1);
+                        float g0 = Rb[u * MT + tok], g1 = Rb[(u + 1) * MT + tok];
+                        float u0 = Rb[(cap + u) * MT + tok], u1 = Rb[(cap + u + 1) * MT + tok];
+                        for (int r = 1; r < S; ++r) {
+                            const float* Rr = Rb + r * rr * MT;
+                            g0 = __fadd_rn(g0, Rr[u * MT + tok]);
+                            g1 = __fadd_rn(g1, Rr[(u + 1) * MT + tok]);
+                            u0 = __fadd_rn(u0, Rr[(cap + u) * MT + tok]);
+                            u1 = __fadd_rn(u1, Rr[(cap + u + 1) * MT + tok]);
+                        }
+                        outv[jj] = pack_bf16x2(silu_mul(bf16_round(g0), bf16_round(u0)),
+                                               silu_mul(bf16_round(g1), bf16_round(u1)));
                     }
                 }
-                consumer_sync();
-                if (tid == 0) mbar_arrive_all_ranks(&pfree[b], S);
+                // the pushers may reuse buffer b (tile rt + 2) once every owner has read it
+                if (rt + 2 < ntl) {
+                    consumer_sync();
+                    if (tid == 0) {
+                        mbar_expect_tx(&rfull[b], recv_bytes);      // armed for tile rt + 2
+                        mbar_arrive_all_ranks(&rfree[b], S);
+                    }
+                }
 #pragma unroll
-                for (int j = 0; j < MAXU; ++j) {
-                    const int u = u_lo + tid + j * kCWarps * 32;
-                    if (u >= u_hi) continue;
-                    const int tok = u / UPT, up = u - tok * UPT;
+                for (int jj = 0; jj < MAXU; ++jj) {
+                    const int q = tid + jj * kCWarps * 32;
+                    if (q >= units) continue;
+                    const int pr = q / MT, tok = q - pr * MT;
                     if (tok >= mvalid) continue;
-                    const int64_t col = (EPI == EPI_STORE) ? (int64_t)kBlock * tile + 2 * up : (int64_t)64 * tile + 2 * up;
-                    *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + col) = outv[j];
+                    const int64_t col = (EPI == EPI_STORE ? (int64_t)kBlock * tile : (int64_t)64 * tile) + 2 * (q0 + pr);
+                    *reinterpret_cast<uint32_t*>(p.y + (int64_t)(m0 + tok) * p.ldy + col) = outv[jj];
                 }
             }
         }
-        // Peers stop touching this CTA's shared memory once every rank has
-        // arrived on its pfree barriers for their last use: wait for those
-        // instead of a cluster-wide barrier at exit.
-        for (int b2 = 0; b2 < 2 && b2 < ntl; ++b2) {
-            const uint32_t last_use = (uint32_t)((ntl - 1 - b2) >> 1);
-            if (!mbar_wait_cluster(&pfree[b2], last_use & 1u)) fail();   // also after an error
+        // Peers touch my shared memory with their pushes (the last tile's have
+        // landed once its rfull wait above completed) and with their arrives on
+        // my rfree barriers, the last of which completes the last round of each
+        // buffer: wait for those rounds before leaving (bounded, also after an
+        // error, when the waits above may have been skipped).
+        if (*vflags != 0 && ntl > 0)
+            (void)mbar_wait_cluster(&rfull[(ntl - 1) & 1], (uint32_t)((ntl - 1) >> 1) & 1u);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            const int rounds = (ntl - 2 - b2 + 1) / 2;       // tiles rt = b2, b2 + 2, ... with rt + 2 < ntl
+            if (rounds > 0 && !mbar_wait_cluster(&rfree[b2], (uint32_t)(rounds - 1) & 1u)) fail();
         }
-    } else {
-        cluster_wait();
     }
     if (warp == kCWarps && lane == 0) {
         // ---- producer steady state (runs ahead across tiles) ----

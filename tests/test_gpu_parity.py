@@ -550,3 +550,76 @@ def test_pdl_dependent_chain_matches_serialised(r9q):
             r9q.r9q_set_pdl(prev)
     assert torch.equal(outs[False].view(torch.int16), outs[True].view(torch.int16))
     assert r9q.r9q_last_device_error() == 0
+
+
+# ------------------------------------------------- decode layer, chained --
+
+def test_decode_layer_chain_graph_pdl_vs_oracle(r9q):
+    """A decode layer's GEMM sequence (QKV projection N=12288, output
+    projection 4096x4096, then the fused expert MLP on the projection's
+    output; attention between them is out of scope) captured in one CUDA graph
+    with programmatic dependent launch on, replayed, and compared with the
+    oracle end to end: every GEMM output within the output bound of the
+    oracle on the same operands, the MLP's fp8 operand hq/hs bit-exact, and
+    the whole replay bit-identical to the same launches serialised (PDL off,
+    no graph)."""
+    M, H, I = 8, 4096, 1536
+    xb = activations_bf16(50, M, H, 0.01, 20.0)
+    wqkv, sqkv = quantised_weights(r9q, 51, 3 * H, H, check_oracle=False)
+    wo, so = quantised_weights(r9q, 52, H, H, check_oracle=False)
+    wgu, sgu = quantised_weights(r9q, 53, 2 * I, H, tensor=1, check_oracle=False)
+    wdn, sdn = quantised_weights(r9q, 53, H, I, tensor=2, check_oracle=False)
+    x = bf16_to_dev(xb)
+
+    def bufs():
+        return {"qkv": torch.empty((M, 3 * H), dtype=torch.bfloat16, device=dev()),
+                "o": torch.empty((M, H), dtype=torch.bfloat16, device=dev()),
+                "h": torch.empty((M, I), dtype=torch.bfloat16, device=dev()),
+                "hq": torch.empty((M, I), dtype=torch.uint8, device=dev()),
+                "hs": torch.empty((M, I // 128), dtype=torch.float32, device=dev()),
+                "y": torch.empty((M, H), dtype=torch.bfloat16, device=dev())}
+
+    def layer(b):
+        r9q.r9q_gemm_fp8_block_qa(x, wqkv, sqkv, y=b["qkv"])
+        r9q.r9q_gemm_fp8_block_qa(x, wo, so, y=b["o"])
+        r9q.r9q_gate_up_swiglu_down(b["o"], wgu, sgu, wdn, sdn, y=b["y"], h=b["h"], hq=b["hq"], hs=b["hs"])
+
+    serial = bufs()
+    prev = r9q.r9q_set_pdl(False)
+    layer(serial)
+    torch.cuda.synchronize()
+    chained = bufs()
+    s = torch.cuda.Stream()
+    r9q.r9q_set_pdl(True)
+    try:
+        with torch.cuda.stream(s):
+            layer(chained)                    # warm-up outside the capture
+        torch.cuda.synchronize()
+        for t in chained.values():
+            t.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer(chained)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+    finally:
+        r9q.r9q_set_pdl(prev)
+    for k in serial:
+        a, b = serial[k], chained[k]
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"{k}: graph + PDL differs from serialised"
+    # end to end against the oracle
+    xq, xs = oracle.quant_group(xb)
+    acc_qkv, _ = oracle.gemm_w8a8(xq, xs, wqkv.cpu().numpy(), sqkv.cpu().numpy())
+    assert_close(bits_of(chained["qkv"]), acc_qkv, "qkv")
+    acc_o, _ = oracle.gemm_w8a8(xq, xs, wo.cpu().numpy(), so.cpu().numpy())
+    o_bits = bits_of(chained["o"])
+    assert_close(o_bits, acc_o, "o")
+    ref = oracle.gate_up_swiglu_down(o_bits, wgu.cpu().numpy(), sgu.cpu().numpy(), wdn.cpu().numpy(),
+                                     sdn.cpu().numpy())
+    assert_close(bits_of(chained["y"]), f32_of_bits(ref["y"]), "y")
+    h_ref = oracle.swiglu_interleaved(bits_of(r9q.r9q_grouped_gemm_fp8(chained["o"], [0, M], wgu[None], sgu[None])))
+    assert np.array_equal(bits_of(chained["h"]), h_ref), "h != oracle SwiGLU of the GPU's g, u"
+    oq, os_ = oracle.quant_group(h_ref)
+    assert np.array_equal(chained["hq"].cpu().numpy(), oq) and np.array_equal(chained["hs"].cpu().numpy(), os_)
+    assert r9q.r9q_last_device_error() == 0

@@ -191,3 +191,4 @@ def test_cpu_tensor_rejected_by_binding():
     import block_scaled_fp8_x128_gb300 as r9q
     with pytest.raises(ValueError):
         r9q.r9q_quant_group128(torch.zeros((1, 128), dtype=torch.bfloat16))
+
