@@ -685,7 +685,8 @@ def profile_case(case, calls):
             r9q.r9q_gate_up_swiglu_down(x, wgu, sgu, wdn, sdn)
     else:
         M, N, K, seed, wonly = {"c1": (16, 4096, 4096, 1, True), "c4-8192": (8192, 4096, 4096, 4, False),
-                                "c4-128": (128, 4096, 4096, 4, False), "c2-16": (16, 12288, 4096, 2, False)}[case]
+                                "c4-128": (128, 4096, 4096, 4, False), "c2-16": (16, 12288, 4096, 2, False),
+                                "c2-1": (1, 12288, 4096, 2, False)}[case]
         copies = max(1, min(8, _copies_for(gemm_bytes(M, N, K))))
         X, W, S, Y = _make_inputs(torch, r9q, "w8a8", M, N, K, seed, 0.0, 1.0, copies, dev)
         for i in range(calls):
@@ -733,7 +734,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     ap.add_argument("--no-pdl", action="store_true", help="launch every GEMM fully serialised")
-    ap.add_argument("--profile-case", choices=["c1", "c4-8192", "c4-128", "c2-16", "c3", "quant-8192"], default=None,
+    ap.add_argument("--profile-case", choices=["c1", "c4-8192", "c4-128", "c2-1", "c2-16", "c3", "quant-8192"],
+                    default=None,
                     help="only run a few calls of one workload (for an external profiler) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
