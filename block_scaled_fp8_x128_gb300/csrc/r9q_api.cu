@@ -256,7 +256,7 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int amode_launch, int sms, Str
     const int mchunks = (int)((M + MT - 1) / MT);
     const int KB = (int)(K / 128);
     const int maxS = KB < kMaxSplits ? KB : kMaxSplits;
-    const int per_sm_cap = MT >= 64 ? 1 : MT >= 32 ? 2 : 3;   // register-limited residency
+    const int per_sm_cap = stream_min_blocks(MT, amode);   // register-limited residency
     const int forced = env_splits();
     // Candidates: S | KB (S <= 8), G | ntiles, ring depth 4..2.  Keep every CTA
     // co-resident; among those take the most CTAs (up to two per SM), then

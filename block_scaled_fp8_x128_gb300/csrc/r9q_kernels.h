@@ -19,6 +19,13 @@ constexpr int kStreamThreads = (kCWarps + 1) * 32;
 constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m3)
 constexpr int kBarBytes = 256;                   // mbarriers + flags
 constexpr int kMaxSplits = 8;                    // cluster size limit (portable)
+// CTAs per SM that the stream kernel's register budget is compiled for, and
+// that the planner counts on (288 threads: 3 CTAs allow 72 registers a
+// thread, 2 allow 112).  W8A8 plans are the same for fused and pre-quantised
+// activations (same summation order), so both use the A_QUANT figure.
+constexpr int stream_min_blocks(int MT, int amode) {
+    return MT >= 64 ? 1 : MT >= 32 ? 2 : (MT >= 16 && amode == A_BF16) ? 2 : 3;
+}
 
 // Split-K exchange of the stream kernel: every rank of a cluster owns a slice
 // of each 128-row tile's outputs and receives every rank's partial of that

@@ -281,23 +281,58 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     }
 
     if (AMODE == A_QUANT) {
-        // In-place group quantisation: one warp walks a token row's groups in
-        // increasing order, so the codes of group g (bytes [128g, 128g+128))
-        // only overwrite bf16 data of groups <= g that it has already read.
-        for (int tok = warp; tok < mvalid; tok += kCWarps + 1) {
+        // In-place group quantisation.  At most one group per warp: each warp
+        // reads one group, the CTA synchronises (the warp alone when a row has
+        // one group), each warp writes that group's codes over the start of
+        // its data.  More groups: each warp walks its
+        // rows, four groups (eight lanes a group) a pass; pass j reads bytes
+        // [1024j, 1024j + 1024) of the row and writes the codes to bytes
+        // [512j, 512j + 512), which only this pass or earlier ones have read,
+        // with all the warp's reads of a pass before its writes.
+        constexpr int W = kCWarps + 1;
+        if (mvalid * nkb <= W) {
+            const bool on = warp < mvalid * nkb;
+            const int tok = on ? warp / nkb : 0, kbl = on ? warp - tok * nkb : 0;
             uint8_t* row = act + tok * act_ld;
-            for (int kbl = 0; kbl < nkb; ++kbl) {
-                const uint2 v = *reinterpret_cast<const uint2*>(row + kbl * 2 * kBlock + 8 * lane);
-                float s;
-                const uint32_t codes =
-                    quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s);
-                __syncwarp();
+            uint2 v = make_uint2(0u, 0u);
+            if (on) v = *reinterpret_cast<const uint2*>(row + kbl * 2 * kBlock + 8 * lane);
+            if (nkb > 1) __syncthreads();   // one group a row: no other warp touches the row
+            else __syncwarp();
+            if (on) {
+                float sc;
+                const uint32_t codes = quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), sc);
                 *reinterpret_cast<uint32_t*>(row + kbl * kBlock + 4 * lane) = codes;
-                if (lane == 0) as_s[tok * kbs_max + kbl] = s;
+                if (lane == 0) as_s[tok * kbs_max + kbl] = sc;
                 if (p.aq != nullptr && group == 0) {
                     const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + 4 * lane;
                     *reinterpret_cast<uint32_t*>(p.aq + off) = codes;
-                    if (lane == 0) p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] = s;
+                    if (lane == 0) p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] = sc;
+                }
+            }
+        } else {
+            const int gl = lane >> 3, el = (lane & 7) * 16;
+            for (int tok = warp; tok < mvalid; tok += W) {
+                uint8_t* row = act + tok * act_ld;
+                for (int kb4 = 0; kb4 < nkb; kb4 += 4) {
+                    const int kbl = kb4 + gl;
+                    uint4 v[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+                    if (kbl < nkb) {
+                        v[0] = *reinterpret_cast<const uint4*>(row + kbl * 2 * kBlock + 2 * el);
+                        v[1] = *reinterpret_cast<const uint4*>(row + kbl * 2 * kBlock + 2 * el + 16);
+                    }
+                    __syncwarp();
+                    float sc;
+                    const uint4 codes = quant_group128_lane8(v, sc);
+                    if (kbl < nkb) {
+                        *reinterpret_cast<uint4*>(row + kbl * kBlock + el) = codes;
+                        if ((lane & 7) == 0) as_s[tok * kbs_max + kbl] = sc;
+                        if (p.aq != nullptr && group == 0) {
+                            const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + el;
+                            *reinterpret_cast<uint4*>(p.aq + off) = codes;
+                            if ((lane & 7) == 0) p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] = sc;
+                        }
+                    }
+                    __syncwarp();
                 }
             }
         }
@@ -539,7 +574,7 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
 }
 
 template <int MT, int AMODE, int EPI>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, AMODE == A_BF16 ? A_BF16 : A_QUANT))
     stream_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p) {
     const int m0 = blockIdx.z * MT;
     stream_gemm_body<MT, AMODE, EPI>(wmap, p, m0, min(MT, p.M - m0), 0, 0);
@@ -551,7 +586,7 @@ __global__ void __launch_bounds__(kStreamThreads)
 // cluster shares blockIdx.z, so all its CTAs leave together, before any
 // cluster barrier.
 template <int MT, int AMODE, int EPI>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, AMODE == A_BF16 ? A_BF16 : A_QUANT))
     stream_grouped_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p,
                           const __grid_constant__ GroupTable gt) {
     const int g = (int)blockIdx.z / gt.zchunks;

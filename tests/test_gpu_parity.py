@@ -219,7 +219,7 @@ def test_w8a8_c4_prefill_sampled(r9q):
     _w8a8_case(r9q, 8192, 4096, 4096, 0.0, 1.0, 4, rows=rows)
 
 
-@pytest.mark.parametrize("M,N,K", [(3, 256, 384), (5, 384, 640), (13, 128, 128), (17, 640, 256),
+@pytest.mark.parametrize("M,N,K", [(3, 256, 384), (5, 384, 640), (4, 256, 2048), (13, 128, 128), (17, 640, 256),
                                    (33, 256, 1152), (63, 384, 512), (65, 256, 512), (100, 128, 384),
                                    (130, 384, 5120),     # tensor-core path (split-K), two scale buffers
                                    (200, 256, 8192),     # ... one scale buffer
