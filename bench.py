@@ -62,7 +62,10 @@ def mlp_bytes(M, H, I, Ho):
 # The sources each timed kernel is built from; a capture under profiles/ only
 # describes the kernel while these files are unchanged.
 KERNEL_SOURCES = {
-    "stream_gemm_kernel": ["r9q_api.cu", "r9q_device.cuh", "r9q_kernels.h", "r9q_stream.cuh", "r9q_stream_bf16.cu"],
+    "stream_sync_kernel": ["r9q_api.cu", "r9q_device.cuh", "r9q_kernels.h", "r9q_stream_common.cuh",
+                           "r9q_stream_sync.cuh", "r9q_stream_launch.cuh", "r9q_stream_bf16.cu"],
+    "stream_gemm_kernel": ["r9q_api.cu", "r9q_device.cuh", "r9q_kernels.h", "r9q_stream_common.cuh",
+                           "r9q_stream.cuh", "r9q_stream_launch.cuh", "r9q_stream_quant.cu"],
     "tc_gemm_kernel": ["r9q_api.cu", "r9q_device.cuh", "r9q_kernels.h", "r9q_tc.cu"],
 }
 
@@ -382,7 +385,7 @@ def run_gpu(args):
                    "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4),
-                     "traffic": captured_traffic("stream_gemm_w8bf16_M16_N4096_K4096.md", "stream_gemm_kernel"),
+                     "traffic": captured_traffic("stream_gemm_w8bf16_M16_N4096_K4096.md", "stream_sync_kernel"),
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback"},
         "e2e": {"value": None if args.no_e2e else round(bpc / (us_e2e * 1e-6) / 1e9, 1), "unit": "GB/s",
                 "us_per_call": None if args.no_e2e else round(us_e2e, 3),

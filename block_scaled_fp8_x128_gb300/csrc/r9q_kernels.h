@@ -13,16 +13,32 @@ enum AMode : int { A_QUANT = 0, A_PREQ = 1, A_BF16 = 2 };
 enum Epi : int { EPI_STORE = 0, EPI_SWIGLU = 1 };
 
 constexpr int kMaxStages = 4;                    // weight ring depth (runtime 2..4)
-constexpr int kRowGroups = 1;                    // 16-row mma groups a consumer warp holds
-constexpr int kCWarps = 8 / kRowGroups;          // consumer (MMA) warps, 16 * kRowGroups weight rows each
-constexpr int kStreamThreads = (kCWarps + 1) * 32;
+constexpr int kCWarps = 8;                       // MMA (mma.sync) or promotion (tcgen05) warps, split-K reduction
+constexpr int kStreamThreads = (kCWarps + 2) * 32;   // tcgen05 body: + the TMA producer warp + the MMA warp
+// Body of the stream GEMM for a token tile: tcgen05 (r9q_stream.cuh) for
+// W8A8 tiles of 16+ rows, where it measured faster; mma.sync
+// (r9q_stream_sync.cuh, (kCWarps + 1) * 32 threads) for 8-row W8A8 tiles,
+// where the tcgen05 issue/commit/wait round trips cost more than the small
+// contraction itself, and for weight-only calls (bf16 activations: the fp8
+// tensor cores would need them re-encoded, which measured slower).
+constexpr bool stream_uses_tc(int MT, int amode) { return amode != A_BF16 && MT >= 16; }
+constexpr int stream_threads(int MT, int amode) {
+    return stream_uses_tc(MT, amode) ? kStreamThreads : (kCWarps + 1) * 32;
+}
 constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m3)
-constexpr int kBarBytes = 256;                   // mbarriers + flags
+constexpr int kBarBytes = 256;                   // mbarriers, TMEM address, flags
 constexpr int kMaxSplits = 8;                    // cluster size limit (portable)
+constexpr int kAccBufs = 4;                      // TMEM k-block partial buffers
+// MMA width N of the token tile (tcgen05 at M = 128 takes N a multiple of 16)
+// and the TMEM columns a CTA allocates (kAccBufs partials, a power of two).
+constexpr int stream_mma_n(int MT) { return MT < 16 ? 16 : MT; }
+constexpr int stream_tmem_cols(int MT) { return kAccBufs * stream_mma_n(MT); }
 // CTAs per SM that the stream kernel's register budget is compiled for, and
-// that the planner counts on (288 threads: 3 CTAs allow 72 registers a
-// thread, 2 allow 112).  W8A8 plans are the same for fused and pre-quantised
-// activations (same summation order), so both use the A_QUANT figure.
+// that the planner counts on (tcgen05 body, 320 threads: 3 CTAs allow 64
+// registers a thread, 2 allow 96; mma.sync body, 288 threads: 72 and 112).  W8A8 plans are the same for fused and pre-quantised
+// activations (same summation order), so both use the A_QUANT figure.  The
+// register budget also bounds the TMEM a SM's resident CTAs hold: at most
+// 3 x 64, 2 x 128 or 1 x 256 columns.
 constexpr int stream_min_blocks(int MT, int amode) {
     return MT >= 64 ? 1 : MT >= 32 ? 2 : (MT >= 16 && amode == A_BF16) ? 2 : 3;
 }

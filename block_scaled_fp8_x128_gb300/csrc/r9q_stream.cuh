@@ -1,124 +1,64 @@
-// Decode-width block-scaled fp8 GEMM ("stream" kernel), sm_103a.
+// Decode-width block-scaled fp8 GEMM ("stream" kernel), tcgen05 body, sm_103a.
 //
 // At decode widths the GEMM is a weight stream: every weight byte is used by a
 // few tokens, so HBM bandwidth bounds it (r9700-stack v0.3.1 notes: the decode
-// GEMMs' weights are the step's largest stream, and fp8 halves it).  This
-// kernel serves W8A8 calls with M <= 32 (larger W8A8 calls go to the tcgen05
-// kernel), and every weight-only and expert-MLP call, in token chunks of up
-// to 64 rows.
+// GEMMs' weights are the step's largest stream, and fp8 halves it).  This body
+// serves W8A8 token tiles of 16 to 64 rows (stream_uses_tc); 8-row tiles and
+// weight-only calls run the mma.sync body (r9q_stream_sync.cuh), which shares
+// the grid, the weight ring and the split-K exchange described here.
 // Design:
 //  * grid (S, G, ceil(M/MT)) launched as clusters of S CTAs along K.  Cluster
 //    g owns the 128-row weight tiles t = g, g+G, g+2G, ... (one scale block
 //    row, or 64 gate + 64 up rows for the SwiGLU epilogue); CTA s of the
 //    cluster owns a contiguous range of 128-wide k-blocks of every such tile.
-//  * one producer thread streams the CTA's 128x128 e4m3 weight tiles with 2-D
-//    TMA (128-byte swizzle) through a shared-memory ring guarded by full/empty
-//    mbarriers, running ahead across tile boundaries.
-//  * the producer thread initialises the ring barriers and issues the weight
-//    stages as its first act, before any block or cluster barrier; the cluster
-//    barrier and the dependency wait (griddepcontrol.wait) come after.  The
-//    CTA's activation slice then arrives in shared memory with one bulk copy
-//    per token row and serves every tile of the CTA.  W8A8: each 128-wide group is quantised in place
-//    once per CTA at the A-load (shuffle amax, fp32-division-exact quotient,
-//    cvt.rn.satfinite.e4m3x2), byte-identical to the standalone quant kernel.
-//    Weight-only: the bf16 rows are the B operand, their pairs swapped in
-//    registers to match the in-register e4m3 -> bf16 conversion.
-//  * eight MMA warps (16 weight rows each; the row-group count kRowGroups
-//    lets a warp hold several 16-row groups that share its activation
-//    fragments, measured slower) run swap-AB mma.sync (weights are the 16-row
-//    A operand, tokens the 8-column B operand): m16n8k32 e4m3 for W8A8,
-//    m16n8k16 bf16 for weight-only.  Each k-block's fp32 partial is
-//    promoted into register accumulators with as[m][kb] * ws[nb][kb] (the
-//    exact block-scaled form: v0.3.0 notes, exact block-scaled fp8 variant).
+//  * warp 8, lane 0 streams the CTA's 128x128 e4m3 weight tiles with 2-D TMA
+//    (128-byte swizzle) through a shared-memory ring guarded by full/empty
+//    mbarriers, running ahead across tile boundaries; it initialises the ring
+//    barriers and issues the first stages as its first act, before any block
+//    or cluster barrier.  The cluster barrier and the dependency wait
+//    (griddepcontrol.wait) come after; the CTA's activation slice then arrives
+//    with one bulk copy per token row.
+//  * the B operand: every warp turns the activation slice into e4m3 rows of a
+//    128-byte-swizzled K-major tile in shared memory (MMA width N = max(MT,
+//    16) rows, zero past the last token), with one scale per (token, k-block).
+//    W8A8: the group-128 quantisation (shuffle amax, fp32-division-exact
+//    quotient, cvt.rn.satfinite.e4m3x2), byte-identical to the standalone
+//    quant kernel; pre-quantised activations are copied into the layout.
+//  * warp 9: TMEM allocation (kAccBufs partial buffers of N fp32 columns) and,
+//    lane 0, the MMAs: per k-block four tcgen05.mma.kind::f8f6f4
+//    M=128 x N x K=32 straight from the TMA stage
+//    and the B tile, committed to the stage's empty barrier and to the
+//    buffer's mdone barrier.
+//  * warps 0..7 (TMEM lane quarter = warp % 4, token columns by warp / 4)
+//    tcgen05.ld each k-block's partial and promote it into register
+//    accumulators with as[m][kb] * ws[nb][kb] (the exact block-scaled form:
+//    v0.3.0 notes, exact block-scaled fp8 variant).
 //  * split-K is reduced through distributed shared memory, pushed: every rank
 //    owns a slice of each tile's output columns (whole column pairs), and each
-//    MMA warp stores its accumulators straight from registers into the owners'
-//    receive buffers with st.async, whose bytes complete on the owner's
-//    mbarrier (no fence or arrive by the pushers); the owner sums its slice
-//    over ranks 0..S-1 in that fixed order (deterministic, no global
-//    workspace).  With several tiles per CTA the receive buffers alternate,
-//    and an owner tells the pushers when a buffer may be refilled.
+//    promoting thread stores its row's accumulators straight from registers
+//    into the owner's receive buffer with st.async, whose bytes complete on
+//    the owner's mbarrier (no fence or arrive by the pushers); the owner sums
+//    its slice over ranks 0..S-1 in that fixed order (deterministic, no
+//    global workspace).  With several tiles per CTA the receive buffers
+//    alternate, and an owner tells the pushers when a buffer may be refilled.
 //  * the epilogue writes bf16 y, or (SwiGLU) rounds gate and up to bf16 and
 //    writes h = bf16(silu(g) * u).
 // Every mbarrier wait is bounded; a timeout records R9Q_ERR_TIMEOUT in the
-// device error word and the kernel drains its copies and returns.
+// device error word and the kernel drains its copies and MMAs, frees its TMEM
+// and returns.
 #pragma once
 
-#include "r9q_device.cuh"
-#include "r9q_kernels.h"
+#include "r9q_stream_common.cuh"
 
 namespace r9q {
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-    }
-    return false;
-}
-
-// Arrive on the barrier at the same shared-memory offset in every CTA of the
-// cluster.  One cluster-scope fence releases everything this CTA did before
-// (the caller synchronises the CTA's writers first); the arrives themselves
-// are relaxed, so the release is paid once rather than once per peer.
-__device__ __forceinline__ void mbar_arrive_all_ranks(uint64_t* local_bar, int S) {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-    const uint32_t a = smem_u32(local_bar);
-    for (int r = 0; r < S; ++r) {
-        const uint32_t addr = dsmem_addr(a, (uint32_t)r);
-        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-    }
-}
-
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
-}
-
-template <int EPI>
-__device__ __forceinline__ void tile_rows(int t, int& r0, int& r1, int& nb0, int& nb1) {
-    if (EPI == EPI_SWIGLU) {
-        const int j = t >> 1, hh = t & 1;
-        r0 = 2 * kBlock * j + 64 * hh;       // gate rows
-        r1 = r0 + kBlock;                    // up rows
-        nb0 = 2 * j;
-        nb1 = 2 * j + 1;
-    } else {
-        r0 = kBlock * t;
-        r1 = r0 + 64;
-        nb0 = nb1 = t;
-    }
-}
-
-// Split-K slices (see stream_recv_rows): pair q of the tile's output columns
-// belongs to rank q * S / NP (NP = 64 row pairs for the plain store, 32 pairs
-// of h columns for SwiGLU); rank r's first pair is ceil(r * NP / S).
-template <int EPI>
-__device__ __forceinline__ int slice_pairs() { return EPI == EPI_SWIGLU ? 32 : 64; }
-template <int EPI>
-__device__ __forceinline__ int slice_first_pair(int r, int S) {
-    return (r * slice_pairs<EPI>() + S - 1) / S;
-}
-// Owner rank of tile row j (0..127) and the row's index in the owner's receive
-// area: plain store, rows 2*first .. in order; SwiGLU, gate rows (j < 64) of
-// the owner's h columns first, then their up rows (index cap + c, where cap =
-// 2 * ceil(32 / S) columns is the most a slice holds).
-template <int EPI>
-__device__ __forceinline__ void slice_of(int j, int S, int& owner, int& u) {
-    if (EPI == EPI_SWIGLU) {
-        const int c = j & 63;
-        owner = (c >> 1) * S / 32;
-        u = (j >> 6) * (2 * ((32 + S - 1) / S)) + c - 2 * slice_first_pair<EPI>(owner, S);
-    } else {
-        owner = (j >> 1) * S / 64;
-        u = j - 2 * slice_first_pair<EPI>(owner, S);
-    }
+// Byte offset of 16-byte chunk ch (k = 16*ch .. 16*ch + 15) of token row tok in
+// k-block kbl of the B operand: per k-block N rows of 128 bytes, 8-row atoms
+// of 1024 bytes with the 128-byte swizzle (chunk index XOR row within the
+// atom), the layout the tensor cores read through umma_sdesc_sw128.
+template <int N>
+__device__ __forceinline__ uint32_t b_offset(int tok, int kbl, int ch) {
+    return (uint32_t)(kbl * (N * 128) + (tok >> 3) * 1024 + (tok & 7) * 128 + ((ch ^ (tok & 7)) << 4));
 }
 
 // The kernel body for the token rows [m0, m0 + mvalid) (mvalid >= 1) of one
@@ -127,7 +67,13 @@ __device__ __forceinline__ void slice_of(int j, int S, int& owner, int& u) {
 template <int MT, int AMODE, int EPI>
 __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const StreamParams& p, const int m0,
                                                  const int mvalid, const int wrow0, const int nbase) {
-    constexpr int NT = MT / 8;
+    constexpr int N = stream_mma_n(MT);                   // MMA width (token columns, zero rows past MT)
+    constexpr int TPW = MT >= 16 ? MT / 2 : 8;            // token columns a promoting thread holds
+    constexpr int NPROMO = MT >= 16 ? kCWarps : 4;        // promoting warps (columns [TPW*(w/4), +TPW))
+    static_assert(AMODE != A_BF16, "weight-only calls run the mma.sync body");
+    constexpr uint32_t kIdesc = umma_idesc_e4m3(128, N);
+    constexpr uint32_t kTmemCols = (uint32_t)stream_tmem_cols(MT);
+    constexpr int kMmaWarp = kCWarps + 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -149,26 +95,28 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     const int iters = ntl * nkb;
 
     // shared memory carve-up (must match stream_smem_bytes)
-    uint8_t* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + nst * kStageBytes);
-    uint64_t* full = bars;                       // [kMaxStages]
-    uint64_t* empty = bars + kMaxStages;         // [kMaxStages]
+    uint8_t* ring = smem;                                        // [nst][128 rows x 128 B] weights
+    uint8_t* bop = smem + nst * kStageBytes;                     // [kbs_max][N rows x 128 B]
+    const int bterm = kbs_max * N * 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bop + bterm);
+    uint64_t* full = bars;                       // [kMaxStages] weight stage landed
+    uint64_t* empty = bars + kMaxStages;         // [kMaxStages] the MMAs reading the stage are done
     uint64_t* abar = bars + 2 * kMaxStages;      // activation bulk copies
     uint64_t* rfull = abar + 1;                  // [2] every rank's slice of a tile has landed in buffer b
     uint64_t* rfree = abar + 3;                  // [2] every rank has summed what I pushed into its buffer b
-    int* flags = reinterpret_cast<int*>(bars + 2 * kMaxStages + 5);   // [0] error, [1] issued
+    uint64_t* mdone = abar + 5;                  // [kAccBufs] TMEM partial buffer holds a finished k-block
+    uint64_t* tfree = mdone + kAccBufs;          // [kAccBufs] the promoting warps have read the buffer
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfree + kAccBufs);
+    int* flags = reinterpret_cast<int*>(tmem_slot + 2);   // [0] error, [1] stages issued, [2] k-blocks committed
     const int rr = stream_recv_rows(S);                               // receive rows per source rank
-    float* R = reinterpret_cast<float*>(smem + nst * kStageBytes + kBarBytes);   // [npbuf][S][rr][MT]
+    float* R = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);   // [npbuf][S][rr][MT]
     const int npbuf = ntl_max > 1 ? 2 : 1;                            // receive buffers
     float* ws_s = R + npbuf * S * rr * MT;                            // [ntl_max][2][kbs_max]
     float* as_s = ws_s + ntl_max * 2 * kbs_max;                       // [MT][kbs_max]
     uintptr_t act_addr = reinterpret_cast<uintptr_t>(as_s + MT * kbs_max);
     uint8_t* act = reinterpret_cast<uint8_t*>((act_addr + 15) & ~static_cast<uintptr_t>(15));
-    // Row stride of the activation slice.  W8A8 (fused): bf16 rows whose first
-    // kslice bytes are overwritten in place by the e4m3 codes; +16 keeps the
-    // code rows on distinct banks for the B-fragment loads.  Weight-only: bf16
-    // rows, +32 for the 8-byte B-fragment loads.  Unfused: e4m3 rows.
-    const int act_ld = (AMODE == A_QUANT) ? (2 * kslice + 16) : (AMODE == A_BF16) ? (2 * kslice + 32) : (kslice + 16);
+    // Activation rows as copied: bf16 (fused quant) or e4m3 codes.
+    const int act_ld = (AMODE == A_PREQ) ? kslice : 2 * kslice;
     const int row_bytes = (AMODE == A_PREQ) ? nkb * kBlock : 2 * nkb * kBlock;   // bytes copied per token
 
     // ---- producer prologue: its barriers, then the weight ring at once ----
@@ -177,11 +125,16 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     if (producer) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCWarps);
+            mbar_init(&empty[s], 1);
         }
         mbar_init(abar, 1);
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(&mdone[b], 1);
+            mbar_init(&tfree[b], NPROMO);
+        }
         flags[0] = 0;
         flags[1] = npro;
+        flags[2] = 0;
         fence_proxy_async_smem();     // the TMA unit sees the initialised ring barriers
         tma_prefetch_desc(&wmap);
         for (int it = 0; it < npro; ++it) {
@@ -204,6 +157,7 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             tma_prefetch_l2_2d(&wmap, (kb0 + i) * kBlock, wrow0 + r1);
         }
     }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     // Bytes this rank receives per tile: every rank's values (all MT tokens)
     // of the rows of my slice (plain store: 2 rows a column pair; SwiGLU: a
     // gate and an up row per h column).
@@ -221,16 +175,21 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
         if (ntl > 0) mbar_expect_tx(&rfull[0], recv_bytes);
         if (ntl > 1) mbar_expect_tx(&rfull[1], recv_bytes);
     }
-    // the MMA warps use the barriers just initialised
+    // the barriers just initialised and the TMEM address are used below
+    umma_fence_before();
     __syncthreads();
+    umma_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
     // Every peer's barriers must exist before anyone arrives on them remotely:
     // arrive on the cluster barrier now, wait for it only just before the
     // first remote access.
     cluster_arrive();
 
     // Weights and their block scales never come from the preceding kernel:
-    // load the scales now.  The activation rows may: prefetch them into L2
-    // only (no stale data can result) and copy them after the wait.
+    // issue the scale loads now (kept in registers) and store them once the
+    // activation copies are under way.  The activation rows may come from the
+    // preceding kernel: prefetch them into L2 only (no stale data can result)
+    // and copy them after the wait.
     if (producer) {
         for (int tok = 0; tok < mvalid; ++tok) {
             const uint8_t* src = (AMODE == A_PREQ)
@@ -239,12 +198,14 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             bulk_prefetch_l2(src, (uint32_t)row_bytes);
         }
     }
-    for (int c = tid; c < ntl * nkb; c += kStreamThreads) {
-        const int tl = c / nkb, i = c - tl * nkb;
+    const int nws = ntl * nkb;
+    float wr0 = 0.0f, wr1 = 0.0f;
+    if (tid < nws) {
+        const int tl = tid / nkb, i = tid - tl * nkb;
         int r0, r1, nb0, nb1;
         tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
-        ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
-        ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
+        wr0 = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
+        wr1 = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
     }
     // every peer's barriers exist (before any remote access below)
     cluster_wait();
@@ -258,20 +219,32 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             bulk_load(act + tok * act_ld, src, (uint32_t)row_bytes, abar);
         }
     }
+    for (int c = tid; c < nws; c += kStreamThreads) {
+        const int tl = c / nkb, i = c - tl * nkb;
+        float v0 = wr0, v1 = wr1;
+        if (c >= kStreamThreads) {
+            int r0, r1, nb0, nb1;
+            tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
+            v0 = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
+            v1 = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
+        }
+        ws_s[(tl * 2 + 0) * kbs_max + i] = v0;
+        ws_s[(tl * 2 + 1) * kbs_max + i] = v1;
+    }
 
-    // rows past the last token: zero codes / activations and zero scales
-    for (int c = tid; c < (MT - mvalid) * (row_bytes / 16); c += kStreamThreads) {
-        const int tok = mvalid + c / (row_bytes / 16), ch = c % (row_bytes / 16);
-        *reinterpret_cast<uint4*>(act + tok * act_ld + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+    // B rows past the last token: zero codes; their scales: zero
+    for (int c = tid; c < nkb * (N - mvalid) * 8; c += kStreamThreads) {
+        const int kbl = c / ((N - mvalid) * 8), r2 = c - kbl * ((N - mvalid) * 8);
+        const int tok = mvalid + (r2 >> 3), ch = r2 & 7;
+        *reinterpret_cast<uint4*>(bop + b_offset<N>(tok, kbl, ch)) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (AMODE == A_PREQ) {
         for (int c = tid; c < MT * nkb; c += kStreamThreads) {
             const int tok = c / nkb, kbl = c - tok * nkb;
             as_s[tok * kbs_max + kbl] = (tok < mvalid) ? p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] : 0.0f;
         }
-    } else if (AMODE == A_QUANT) {
-        // only the padding rows: the scales of rows < mvalid are written by the
-        // quant loop below, which other warps may already be running
+    } else {
+        // only the padding rows: the scales of rows < mvalid are written below
         for (int c = tid; c < (MT - mvalid) * nkb; c += kStreamThreads)
             as_s[(mvalid + c / nkb) * kbs_max + c % nkb] = 0.0f;
     }
@@ -280,28 +253,19 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
         atomicExch(&flags[0], 1);
     }
 
+    // ---- the B operand: the CTA's activation slice as e4m3, in the swizzled
+    // layout, with its scale per (token, k-block) in as_s ----
+    constexpr int W = kCWarps + 2;
     if (AMODE == A_QUANT) {
-        // In-place group quantisation.  At most one group per warp: each warp
-        // reads one group, the CTA synchronises (the warp alone when a row has
-        // one group), each warp writes that group's codes over the start of
-        // its data.  More groups: each warp walks its
-        // rows, four groups (eight lanes a group) a pass; pass j reads bytes
-        // [1024j, 1024j + 1024) of the row and writes the codes to bytes
-        // [512j, 512j + 512), which only this pass or earlier ones have read,
-        // with all the warp's reads of a pass before its writes.
-        constexpr int W = kCWarps + 1;
+        // Group-128 quantisation.  At most one group per warp: each warp takes
+        // one group; otherwise four groups a warp pass, eight lanes a group.
         if (mvalid * nkb <= W) {
-            const bool on = warp < mvalid * nkb;
-            const int tok = on ? warp / nkb : 0, kbl = on ? warp - tok * nkb : 0;
-            uint8_t* row = act + tok * act_ld;
-            uint2 v = make_uint2(0u, 0u);
-            if (on) v = *reinterpret_cast<const uint2*>(row + kbl * 2 * kBlock + 8 * lane);
-            if (nkb > 1) __syncthreads();   // one group a row: no other warp touches the row
-            else __syncwarp();
-            if (on) {
+            if (warp < mvalid * nkb) {
+                const int tok = warp / nkb, kbl = warp - tok * nkb;
+                const uint2 v = *reinterpret_cast<const uint2*>(act + tok * act_ld + kbl * 2 * kBlock + 8 * lane);
                 float sc;
                 const uint32_t codes = quant_group128_warp(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), sc);
-                *reinterpret_cast<uint32_t*>(row + kbl * kBlock + 4 * lane) = codes;
+                *reinterpret_cast<uint32_t*>(bop + b_offset<N>(tok, kbl, lane >> 2) + 4 * (lane & 3)) = codes;
                 if (lane == 0) as_s[tok * kbs_max + kbl] = sc;
                 if (p.aq != nullptr && group == 0) {
                     const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + 4 * lane;
@@ -311,158 +275,137 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             }
         } else {
             const int gl = lane >> 3, el = (lane & 7) * 16;
-            for (int tok = warp; tok < mvalid; tok += W) {
-                uint8_t* row = act + tok * act_ld;
-                for (int kb4 = 0; kb4 < nkb; kb4 += 4) {
-                    const int kbl = kb4 + gl;
-                    uint4 v[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-                    if (kbl < nkb) {
-                        v[0] = *reinterpret_cast<const uint4*>(row + kbl * 2 * kBlock + 2 * el);
-                        v[1] = *reinterpret_cast<const uint4*>(row + kbl * 2 * kBlock + 2 * el + 16);
+            const int ngroups = mvalid * nkb, nquads = (ngroups + 3) >> 2;
+            for (int qd = warp; qd < nquads; qd += W) {
+                const int gi = qd * 4 + gl;
+                const bool on = gi < ngroups;
+                const int tok = on ? gi / nkb : 0, kbl = on ? gi - tok * nkb : 0;
+                uint4 v[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+                if (on) {
+                    v[0] = *reinterpret_cast<const uint4*>(act + tok * act_ld + kbl * 2 * kBlock + 2 * el);
+                    v[1] = *reinterpret_cast<const uint4*>(act + tok * act_ld + kbl * 2 * kBlock + 2 * el + 16);
+                }
+                float sc;
+                const uint4 codes = quant_group128_lane8(v, sc);
+                if (on) {
+                    *reinterpret_cast<uint4*>(bop + b_offset<N>(tok, kbl, lane & 7)) = codes;
+                    if ((lane & 7) == 0) as_s[tok * kbs_max + kbl] = sc;
+                    if (p.aq != nullptr && group == 0) {
+                        const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + el;
+                        *reinterpret_cast<uint4*>(p.aq + off) = codes;
+                        if ((lane & 7) == 0) p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] = sc;
                     }
-                    __syncwarp();
-                    float sc;
-                    const uint4 codes = quant_group128_lane8(v, sc);
-                    if (kbl < nkb) {
-                        *reinterpret_cast<uint4*>(row + kbl * kBlock + el) = codes;
-                        if ((lane & 7) == 0) as_s[tok * kbs_max + kbl] = sc;
-                        if (p.aq != nullptr && group == 0) {
-                            const int64_t off = (int64_t)(m0 + tok) * p.K + (int64_t)(kb0 + kbl) * kBlock + el;
-                            *reinterpret_cast<uint4*>(p.aq + off) = codes;
-                            if ((lane & 7) == 0) p.as[(int64_t)(m0 + tok) * KB + kb0 + kbl] = sc;
-                        }
-                    }
-                    __syncwarp();
                 }
             }
         }
+    } else {
+        // pre-quantised codes: copied rows -> swizzled layout
+        for (int c = tid; c < mvalid * nkb * 8; c += kStreamThreads) {
+            const int tok = c / (nkb * 8), r = c - tok * (nkb * 8), kbl = r >> 3, ch = r & 7;
+            *reinterpret_cast<uint4*>(bop + b_offset<N>(tok, kbl, ch)) =
+                *reinterpret_cast<const uint4*>(act + tok * act_ld + kbl * kBlock + ch * 16);
+        }
     }
+    // the tensor cores read B through the async proxy
+    fence_proxy_async_smem();
     __syncthreads();
 
-    const int g = lane >> 2, t = lane & 3;
+    volatile int* vflags = flags;
+    auto fail = [&]() {
+        record_error(p.err, kErrTimeout);
+        atomicExch(&flags[0], 1);
+    };
+
+    if (warp == kMmaWarp) {
+        // ---- MMA issuer: k-block it of tile it / nkb into TMEM buffer it % kAccBufs ----
+        if (lane == 0) {
+            int committed = 0;
+            for (int it = 0; it < iters; ++it) {
+                if (*vflags != 0) break;
+                const int tl = it / nkb, i = it - tl * nkb, st = it % nst, b = it % kAccBufs;
+                (void)tl;
+                if (!mbar_wait(&full[st], (uint32_t)(it / nst) & 1u)) {
+                    fail();
+                    break;
+                }
+                if (it >= kAccBufs && !mbar_wait(&tfree[b], (uint32_t)(it / kAccBufs - 1) & 1u)) {
+                    fail();
+                    break;
+                }
+                umma_fence_after();
+                const uint32_t td = tmem_base + (uint32_t)(b * N);
+                const uint32_t sa = smem_u32(ring + st * kStageBytes);
+                const uint32_t sb = smem_u32(bop + i * (N * 128));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_e4m3(td, umma_sdesc_sw128(sa + 32 * k), umma_sdesc_sw128(sb + 32 * k), kIdesc, k ? 1u : 0u);
+                umma_commit(&empty[st]);      // the stage may be refilled once these MMAs are done
+                umma_commit(&mdone[b]);
+                committed = it + 1;
+            }
+            flags[2] = committed;
+            // After an error the promoting warps stop waiting: let the MMAs
+            // issued finish before the TMEM is released (bounded).
+            if (*vflags != 0 && committed > 0) {
+                const int last = committed - 1;
+                (void)mbar_wait(&mdone[last % kAccBufs], (uint32_t)(last / kAccBufs) & 1u);
+            }
+        }
+        __syncwarp();
+    }
+
     if (warp < kCWarps) {
-        // ---- MMA warps: rows [16*RG*warp, 16*RG*(warp + 1)) of every tile, as
-        // RG 16-row groups that share every activation fragment the warp loads ----
-        constexpr int RG = kRowGroups;
-        const int box = (warp * 16 * RG) >> 6;           // 64-row half: scale row nb0 or nb1
-        const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int lchk = lane >> 4;
+        // ---- promotion: warp w reads TMEM lanes 32*(w%4) .. +31 (tile rows)
+        // and token columns [TPW*(w/4), +TPW); each k-block's partial is
+        // promoted into register accumulators with as[m][kb] * ws[nb][kb] ----
+        const bool promo = warp < NPROMO;
+        const int row = 32 * (warp & 3) + lane;                 // weight tile row = TMEM lane
+        const int cb = (warp >> 2) * TPW;                       // first token column
+        const int box = row >> 6;                               // 64-row half: scale row nb0 or nb1
+        const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
         // A failed wait sets flags[0]; from then on every wait is skipped but
-        // all MMA warps keep walking the same loop and barrier sequence, so no
+        // all warps keep walking the same loop and barrier sequence, so no
         // warp is left waiting at a named barrier.
-        volatile int* vflags = flags;
-        auto fail = [&]() {
-            record_error(p.err, kErrTimeout);
-            atomicExch(&flags[0], 1);
-        };
         // Tile tl's partial is pushed, then tile tl-1 is reduced: the wait for
         // the peers' partials of one tile overlaps the MMAs of the next.
         for (int tl = 0; tl <= ntl; ++tl) {
-            if (tl < ntl) {
-                float acc[RG][NT][4];
+            if (tl < ntl && promo) {
+                float acc[TPW];
 #pragma unroll
-                for (int rg = 0; rg < RG; ++rg)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[rg][nt][e] = 0.0f;
+                for (int j = 0; j < TPW; ++j) acc[j] = 0.0f;
                 const float* wsv_s = ws_s + (tl * 2 + box) * kbs_max;
                 for (int i = 0; i < nkb; ++i) {
-                    const int it = tl * nkb + i;
-                    const int st = it % nst;
-                    if (*vflags == 0 && !mbar_wait(&full[st], (uint32_t)(it / nst) & 1u)) fail();
-                    const uint32_t tbase = smem_u32(ring + st * kStageBytes);
-                    float d[RG][NT][4];
-#pragma unroll
-                    for (int rg = 0; rg < RG; ++rg)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) d[rg][nt][e] = 0.0f;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const int chunk = ks * 2 + lchk;
-                        uint32_t a[RG][4];
-#pragma unroll
-                        for (int rg = 0; rg < RG; ++rg) {
-                            const int row = warp * 16 * RG + rg * 16 + lrow;
-                            ldmatrix_x4(tbase + row * 128 + ((chunk ^ (row & 7)) << 4), a[rg][0], a[rg][1], a[rg][2],
-                                        a[rg][3]);
-                        }
-                        if (AMODE != A_BF16) {
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const uint8_t* bp = act + (nt * 8 + g) * act_ld + i * kBlock + ks * 32 + 4 * t;
-                                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp);
-                                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 16);
-#pragma unroll
-                                for (int rg = 0; rg < RG; ++rg) mma_e4m3_16832(d[rg][nt], a[rg], b0, b1);
-                            }
-                        } else {
-                            uint32_t ev[RG][4], od[RG][4];
-#pragma unroll
-                            for (int rg = 0; rg < RG; ++rg)
-#pragma unroll
-                                for (int r = 0; r < 4; ++r) e4m3x4_to_bf16x2x2(a[rg][r], ev[rg][r], od[rg][r]);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const uint8_t* bp = act + (nt * 8 + g) * act_ld + 2 * (i * kBlock + ks * 32 + 4 * t);
-                                // (x0,x1),(x2,x3) -> (x0,x2),(x1,x3): the pairing of e4m3x4_to_bf16x2x2
-                                const uint2 bv = *reinterpret_cast<const uint2*>(bp);
-                                const uint2 cv = *reinterpret_cast<const uint2*>(bp + 32);
-                                const uint32_t b0 = __byte_perm(bv.x, bv.y, 0x5410), b1 = __byte_perm(bv.x, bv.y, 0x7632);
-                                const uint32_t c0 = __byte_perm(cv.x, cv.y, 0x5410), c1 = __byte_perm(cv.x, cv.y, 0x7632);
-#pragma unroll
-                                for (int rg = 0; rg < RG; ++rg) {
-                                    mma_bf16_16816(d[rg][nt], ev[rg][0], ev[rg][1], od[rg][0], od[rg][1], b0, b1);
-                                    mma_bf16_16816(d[rg][nt], ev[rg][2], ev[rg][3], od[rg][2], od[rg][3], c0, c1);
-                                }
-                            }
-                        }
-                    }
+                    const int it = tl * nkb + i, b = it % kAccBufs;
+                    if (*vflags == 0 && !mbar_wait(&mdone[b], (uint32_t)(it / kAccBufs) & 1u)) fail();
+                    umma_fence_after();
+                    float d[TPW];
+                    tmem_ld<TPW>(tmem_base + tlane + (uint32_t)(b * N + cb), d);
+                    tmem_wait_ld(d);
+                    umma_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);
-                    // block-scale promotion of this k-block's partial
+                    if (lane == 0) mbar_arrive(&tfree[b]);
                     const float wsv = wsv_s[i];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        float sc0 = wsv, sc1 = wsv;
-                        if (AMODE != A_BF16) {
-                            sc0 = as_s[(nt * 8 + 2 * t) * kbs_max + i] * wsv;
-                            sc1 = as_s[(nt * 8 + 2 * t + 1) * kbs_max + i] * wsv;
-                        }
-#pragma unroll
-                        for (int rg = 0; rg < RG; ++rg) {
-                            acc[rg][nt][0] = fmaf(d[rg][nt][0], sc0, acc[rg][nt][0]);
-                            acc[rg][nt][1] = fmaf(d[rg][nt][1], sc1, acc[rg][nt][1]);
-                            acc[rg][nt][2] = fmaf(d[rg][nt][2], sc0, acc[rg][nt][2]);
-                            acc[rg][nt][3] = fmaf(d[rg][nt][3], sc1, acc[rg][nt][3]);
-                        }
-                    }
+                    for (int j = 0; j < TPW; ++j)
+                        acc[j] = fmaf(d[j], as_s[(cb + j) * kbs_max + i] * wsv, acc[j]);
                 }
 
-                // ---- push the tile's partial to the ranks that own its rows ----
-                // into buffer b = tl & 1 of each owner, once every owner has
+                // ---- push the row's partial to the rank that owns it ----
+                // into buffer b = tl & 1 of the owner, once every owner has
                 // summed what was pushed there two tiles ago; the stores count
                 // their bytes on the owner's rfull[b]
                 const int b = tl & 1;
                 const uint32_t use = (uint32_t)(tl >> 1);
                 if (tl >= 2 && *vflags == 0 && !mbar_wait_cluster(&rfree[b], (use - 1) & 1u)) fail();
                 const uint32_t rbase = smem_u32(R + (size_t)b * S * rr * MT) + (uint32_t)(split * rr * MT * 4);
-                const uint32_t rbar = smem_u32(&rfull[b]);
+                int owner, u;
+                slice_of<EPI>(row, S, owner, u);
+                const uint32_t dst = dsmem_addr(rbase + (uint32_t)((u * MT + cb) * 4), (uint32_t)owner);
+                const uint32_t dbar = dsmem_addr(smem_u32(&rfull[b]), (uint32_t)owner);
 #pragma unroll
-                for (int rg = 0; rg < RG; ++rg)
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
-                        int owner, u;
-                        slice_of<EPI>(warp * 16 * RG + rg * 16 + g + 8 * h8, S, owner, u);
-                        const uint32_t dst = dsmem_addr(rbase + (uint32_t)(u * MT * 4), (uint32_t)owner);
-                        const uint32_t dbar = dsmem_addr(rbar, (uint32_t)owner);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            st_async_f32x2(dst + (uint32_t)((nt * 8 + 2 * t) * 4), acc[rg][nt][2 * h8],
-                                           acc[rg][nt][2 * h8 + 1], dbar);
-                    }
+                for (int c4 = 0; c4 < TPW / 4; ++c4)
+                    st_async_f32x4(dst + (uint32_t)(16 * c4), acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2],
+                                   acc[4 * c4 + 3], dbar);
             }
             if (tl >= 1) {
                 // ---- tile rt: sum my slice over the ranks 0..S-1, in that order ----
@@ -562,8 +505,8 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
         }
         flags[1] = issued;
     }
+    umma_fence_before();
     __syncthreads();
-
     // After an error, wait (bounded) for every copy still in flight before the
     // CTA exits.
     if (flags[0] != 0 && tid == 0) {
@@ -571,10 +514,14 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
         for (int it = max(0, issued - nst); it < issued; ++it)
             (void)mbar_wait(&full[it % nst], (uint32_t)(it / nst) & 1u);
     }
+    if (warp == kMmaWarp) {
+        umma_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
 }
 
 template <int MT, int AMODE, int EPI>
-__global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, AMODE == A_BF16 ? A_BF16 : A_QUANT))
+__global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, A_QUANT))
     stream_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p) {
     const int m0 = blockIdx.z * MT;
     stream_gemm_body<MT, AMODE, EPI>(wmap, p, m0, min(MT, p.M - m0), 0, 0);
@@ -586,7 +533,7 @@ __global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, AMODE ==
 // cluster shares blockIdx.z, so all its CTAs leave together, before any
 // cluster barrier.
 template <int MT, int AMODE, int EPI>
-__global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, AMODE == A_BF16 ? A_BF16 : A_QUANT))
+__global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, A_QUANT))
     stream_grouped_kernel(const __grid_constant__ CUtensorMap wmap, const StreamParams p,
                           const __grid_constant__ GroupTable gt) {
     const int g = (int)blockIdx.z / gt.zchunks;
@@ -594,51 +541,6 @@ __global__ void __launch_bounds__(kStreamThreads, stream_min_blocks(MT, AMODE ==
     const int mvalid = min(MT, gt.off[g + 1] - m0);
     if (mvalid <= 0) return;
     stream_gemm_body<MT, AMODE, EPI>(wmap, p, m0, mvalid, g * gt.wrows, g * (gt.wrows / kBlock));
-}
-
-template <int AMODE>
-cudaError_t launch_stream_impl(const StreamPlan& plan, int epi, const CUtensorMap& wmap,
-                               const StreamParams& p, cudaStream_t st, bool pdl) {
-    void (*kern)(const CUtensorMap, const StreamParams) = nullptr;
-    if (epi == EPI_STORE) {
-        switch (plan.MT) {
-            case 8: kern = stream_gemm_kernel<8, AMODE, EPI_STORE>; break;
-            case 16: kern = stream_gemm_kernel<16, AMODE, EPI_STORE>; break;
-            case 32: kern = stream_gemm_kernel<32, AMODE, EPI_STORE>; break;
-            case 64: kern = stream_gemm_kernel<64, AMODE, EPI_STORE>; break;
-            default: return cudaErrorInvalidValue;
-        }
-    } else {
-        if (AMODE == A_PREQ) return cudaErrorInvalidValue;
-        switch (plan.MT) {
-            case 8: kern = stream_gemm_kernel<8, AMODE, EPI_SWIGLU>; break;
-            case 16: kern = stream_gemm_kernel<16, AMODE, EPI_SWIGLU>; break;
-            case 32: kern = stream_gemm_kernel<32, AMODE, EPI_SWIGLU>; break;
-            case 64: kern = stream_gemm_kernel<64, AMODE, EPI_SWIGLU>; break;
-            default: return cudaErrorInvalidValue;
-        }
-    }
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), plan.smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.splits, (unsigned)plan.groups, (unsigned)plan.mchunks);
-    cfg.blockDim = dim3(kStreamThreads, 1, 1);
-    cfg.dynamicSmemBytes = plan.smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[2];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = (unsigned)plan.splits;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    int nattr = 1;
-    if (pdl) {
-        attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attrs[1].val.programmaticStreamSerializationAllowed = 1;
-        nattr = 2;
-    }
-    cfg.attrs = attrs;
-    cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, kern, wmap, p);
 }
 
 }  // namespace r9q

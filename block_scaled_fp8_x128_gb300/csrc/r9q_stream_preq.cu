@@ -1,6 +1,6 @@
 // Instantiations of the decode-width stream GEMM for the A_PREQ A-load
 // (one translation unit per A-load mode so the library builds in parallel).
-#include "r9q_stream.cuh"
+#include "r9q_stream_launch.cuh"
 
 namespace r9q {
 
