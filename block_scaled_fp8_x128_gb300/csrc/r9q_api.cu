@@ -237,19 +237,23 @@ size_t mlp_workspace(int64_t M, int64_t I, int flags, bool have_h, bool have_hq)
 // ------------------------------------------------------------ planning --
 
 size_t stream_smem_bytes(int MT, int amode, int S, int kbs_max, int ntl_max, int stages) {
-    // The kernel's carve-up, in order: weight ring, [tcgen05: B operand,
-    // 1024-aligned after the ring], barriers, receive buffers, scales,
-    // activation rows.
     const size_t kslice = (size_t)kbs_max * 128;
-    const bool tc = stream_uses_tc(MT, amode);
-    const size_t bop = tc ? kslice * (size_t)stream_mma_n(MT) : 0;
-    // activation row stride: tcgen05, as copied; mma.sync, padded so the
-    // B-fragment loads of the rows fall on distinct banks
-    const size_t act_ld = tc ? ((amode == A_PREQ) ? kslice : 2 * kslice)
-                             : ((amode == A_QUANT) ? 2 * kslice + 16 : (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16);
     const size_t npbuf = ntl_max > 1 ? 2 : 1;
-    size_t off = (size_t)stages * kStageBytes + bop + kBarBytes + npbuf * (size_t)S * stream_recv_rows(S) * MT * 4 +
-                 4 * ((size_t)ntl_max * 2 * kbs_max + (size_t)MT * kbs_max);
+    const size_t recv = npbuf * (size_t)S * stream_recv_rows(S) * MT * 4;
+    const size_t scales = 4 * ((size_t)ntl_max * 2 * kbs_max + (size_t)MT * kbs_max);
+    if (stream_uses_tc(MT, amode)) {
+        // tcgen05 body, in order: weight ring, activation rows (later more
+        // ring stages), B tile, barriers, receive buffers, scales; the first
+        // three stay 1024-aligned
+        const size_t act = (size_t)MT * ((amode == A_PREQ) ? kslice : 2 * kslice);
+        const size_t bop = kslice * (size_t)stream_mma_n(MT);
+        return 1024 + (size_t)stages * kStageBytes + act + bop + kBarBytes + recv + scales;
+    }
+    // mma.sync body, in order: weight ring, barriers, receive buffers, scales,
+    // activation rows (padded so the B-fragment loads of the rows fall on
+    // distinct banks)
+    const size_t act_ld = (amode == A_QUANT) ? 2 * kslice + 16 : (amode == A_BF16) ? 2 * kslice + 32 : kslice + 16;
+    size_t off = (size_t)stages * kStageBytes + kBarBytes + recv + scales;
     off = (off + 15) & ~static_cast<size_t>(15);
     return 1024 + off + (size_t)MT * act_ld;
 }

@@ -29,6 +29,11 @@ constexpr int kStageBytes = 128 * 128;           // 128 weight rows x 128 k (e4m
 constexpr int kBarBytes = 256;                   // mbarriers, TMEM address, flags
 constexpr int kMaxSplits = 8;                    // cluster size limit (portable)
 constexpr int kAccBufs = 4;                      // TMEM k-block partial buffers
+constexpr int kMaxRing = 8;                      // tcgen05 body: ring stages incl. the reused activation area
+// tcgen05 body barrier area: full/empty per ring stage, the activation copy,
+// rfull[2], rfree[2], mdone/tfree per TMEM buffer; then the TMEM address and
+// three flags.
+static_assert((2 * kMaxRing + 5 + 2 * kAccBufs) * 8 + 8 + 12 <= kBarBytes, "stream barrier area");
 // MMA width N of the token tile (tcgen05 at M = 128 takes N a multiple of 16)
 // and the TMEM columns a CTA allocates (kAccBufs partials, a power of two).
 constexpr int stream_mma_n(int MT) { return MT < 16 ? 16 : MT; }

@@ -94,14 +94,21 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     const int ntl_max = (p.ntiles + G - 1) / G;
     const int iters = ntl * nkb;
 
+    // Activation rows as copied: bf16 (fused quant) or e4m3 codes.
+    const int act_ld = (AMODE == A_PREQ) ? kslice : 2 * kslice;
+    const int act_bytes = MT * act_ld;                           // a multiple of 1024
     // shared memory carve-up (must match stream_smem_bytes)
     uint8_t* ring = smem;                                        // [nst][128 rows x 128 B] weights
-    uint8_t* bop = smem + nst * kStageBytes;                     // [kbs_max][N rows x 128 B]
+    uint8_t* act = smem + nst * kStageBytes;                     // [MT][act_ld] activation rows
+    uint8_t* bop = act + act_bytes;                              // [kbs_max][N rows x 128 B]
+    // Once the B tile is built the activation rows are dead: their space
+    // continues the ring (stages nst .. ntot-1, used from the first refill on).
+    const int ntot = min(nst + act_bytes / kStageBytes, kMaxRing);
     const int bterm = kbs_max * N * 128;
     uint64_t* bars = reinterpret_cast<uint64_t*>(bop + bterm);
-    uint64_t* full = bars;                       // [kMaxStages] weight stage landed
-    uint64_t* empty = bars + kMaxStages;         // [kMaxStages] the MMAs reading the stage are done
-    uint64_t* abar = bars + 2 * kMaxStages;      // activation bulk copies
+    uint64_t* full = bars;                       // [kMaxRing] weight stage landed
+    uint64_t* empty = bars + kMaxRing;           // [kMaxRing] the MMAs reading the stage are done
+    uint64_t* abar = bars + 2 * kMaxRing;        // activation bulk copies
     uint64_t* rfull = abar + 1;                  // [2] every rank's slice of a tile has landed in buffer b
     uint64_t* rfree = abar + 3;                  // [2] every rank has summed what I pushed into its buffer b
     uint64_t* mdone = abar + 5;                  // [kAccBufs] TMEM partial buffer holds a finished k-block
@@ -113,17 +120,13 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     const int npbuf = ntl_max > 1 ? 2 : 1;                            // receive buffers
     float* ws_s = R + npbuf * S * rr * MT;                            // [ntl_max][2][kbs_max]
     float* as_s = ws_s + ntl_max * 2 * kbs_max;                       // [MT][kbs_max]
-    uintptr_t act_addr = reinterpret_cast<uintptr_t>(as_s + MT * kbs_max);
-    uint8_t* act = reinterpret_cast<uint8_t*>((act_addr + 15) & ~static_cast<uintptr_t>(15));
-    // Activation rows as copied: bf16 (fused quant) or e4m3 codes.
-    const int act_ld = (AMODE == A_PREQ) ? kslice : 2 * kslice;
     const int row_bytes = (AMODE == A_PREQ) ? nkb * kBlock : 2 * nkb * kBlock;   // bytes copied per token
 
     // ---- producer prologue: its barriers, then the weight ring at once ----
     const bool producer = (warp == kCWarps && lane == 0);
     const int npro = min(iters, nst);
     if (producer) {
-        for (int s = 0; s < nst; ++s) {
+        for (int s = 0; s < ntot; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -322,9 +325,9 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             int committed = 0;
             for (int it = 0; it < iters; ++it) {
                 if (*vflags != 0) break;
-                const int tl = it / nkb, i = it - tl * nkb, st = it % nst, b = it % kAccBufs;
+                const int tl = it / nkb, i = it - tl * nkb, st = it % ntot, b = it % kAccBufs;
                 (void)tl;
-                if (!mbar_wait(&full[st], (uint32_t)(it / nst) & 1u)) {
+                if (!mbar_wait(&full[st], (uint32_t)(it / ntot) & 1u)) {
                     fail();
                     break;
                 }
@@ -482,11 +485,12 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     }
     if (warp == kCWarps && lane == 0) {
         // ---- producer steady state (runs ahead across tiles) ----
+        // (after the B tile is built: the stages past nst are free from here on)
         int issued = npro;
         int cur_tl = -1, r0 = 0, r1 = 0, nb0, nb1;
-        for (int it = nst; it < iters; ++it) {
-            const int st = it % nst;
-            if (!mbar_wait(&empty[st], ((uint32_t)(it / nst) & 1u) ^ 1u)) {
+        for (int it = npro; it < iters; ++it) {
+            const int st = it % ntot;
+            if (it >= ntot && !mbar_wait(&empty[st], ((uint32_t)(it / ntot) & 1u) ^ 1u)) {
                 record_error(p.err, kErrTimeout);
                 atomicExch(&flags[0], 1);
                 break;
@@ -511,8 +515,8 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     // CTA exits.
     if (flags[0] != 0 && tid == 0) {
         const int issued = flags[1];
-        for (int it = max(0, issued - nst); it < issued; ++it)
-            (void)mbar_wait(&full[it % nst], (uint32_t)(it / nst) & 1u);
+        for (int it = max(0, issued - ntot); it < issued; ++it)
+            (void)mbar_wait(&full[it % ntot], (uint32_t)(it / ntot) & 1u);
     }
     if (warp == kMmaWarp) {
         umma_fence_after();
