@@ -334,6 +334,12 @@ __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrive without release semantics: enough where the only thing peers rely on
+// is mbarrier initialisation, which fence_mbar_init (release at cluster
+// scope) has already ordered before this arrive.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

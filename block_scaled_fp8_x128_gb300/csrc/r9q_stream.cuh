@@ -185,8 +185,10 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     const uint32_t tmem_base = *tmem_slot;
     // Every peer's barriers must exist before anyone arrives on them remotely:
     // arrive on the cluster barrier now, wait for it only just before the
-    // first remote access.
-    cluster_arrive();
+    // first remote access.  Peers touch nothing of this CTA but those barriers
+    // and the receive buffers they write, so the arrive is relaxed: the
+    // initialisation is released by fence_mbar_init above.
+    cluster_arrive_relaxed();
 
     // Weights and their block scales never come from the preceding kernel:
     // issue the scale loads now (kept in registers) and store them once the

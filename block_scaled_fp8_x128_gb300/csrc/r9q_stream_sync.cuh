@@ -157,8 +157,10 @@ __device__ __forceinline__ void stream_sync_body(const CUtensorMap& wmap, const 
     __syncthreads();
     // Every peer's barriers must exist before anyone arrives on them remotely:
     // arrive on the cluster barrier now, wait for it only just before the
-    // first remote access.
-    cluster_arrive();
+    // first remote access.  Peers touch nothing of this CTA but those barriers
+    // and the receive buffers they write, so the arrive is relaxed: the
+    // initialisation is released by fence_mbar_init above.
+    cluster_arrive_relaxed();
 
     // Weights and their block scales never come from the preceding kernel:
     // load the scales now.  The activation rows may: prefetch them into L2
