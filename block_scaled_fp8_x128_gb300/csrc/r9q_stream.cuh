@@ -191,10 +191,8 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
     cluster_arrive_relaxed();
 
     // Weights and their block scales never come from the preceding kernel:
-    // issue the scale loads now (kept in registers) and store them once the
-    // activation copies are under way.  The activation rows may come from the
-    // preceding kernel: prefetch them into L2 only (no stale data can result)
-    // and copy them after the wait.
+    // load the scales now.  The activation rows may: prefetch them into L2
+    // only (no stale data can result) and copy them after the wait.
     if (producer) {
         for (int tok = 0; tok < mvalid; ++tok) {
             const uint8_t* src = (AMODE == A_PREQ)
@@ -204,13 +202,12 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
         }
     }
     const int nws = ntl * nkb;
-    float wr0 = 0.0f, wr1 = 0.0f;
-    if (tid < nws) {
-        const int tl = tid / nkb, i = tid - tl * nkb;
+    for (int c = tid; c < nws; c += kStreamThreads) {
+        const int tl = c / nkb, i = c - tl * nkb;
         int r0, r1, nb0, nb1;
         tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
-        wr0 = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
-        wr1 = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
+        ws_s[(tl * 2 + 0) * kbs_max + i] = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
+        ws_s[(tl * 2 + 1) * kbs_max + i] = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
     }
     // every peer's barriers exist (before any remote access below)
     cluster_wait();
@@ -224,19 +221,6 @@ __device__ __forceinline__ void stream_gemm_body(const CUtensorMap& wmap, const 
             bulk_load(act + tok * act_ld, src, (uint32_t)row_bytes, abar);
         }
     }
-    for (int c = tid; c < nws; c += kStreamThreads) {
-        const int tl = c / nkb, i = c - tl * nkb;
-        float v0 = wr0, v1 = wr1;
-        if (c >= kStreamThreads) {
-            int r0, r1, nb0, nb1;
-            tile_rows<EPI>(group + tl * G, r0, r1, nb0, nb1);
-            v0 = p.ws[(int64_t)(nbase + nb0) * KB + kb0 + i];
-            v1 = p.ws[(int64_t)(nbase + nb1) * KB + kb0 + i];
-        }
-        ws_s[(tl * 2 + 0) * kbs_max + i] = v0;
-        ws_s[(tl * 2 + 1) * kbs_max + i] = v1;
-    }
-
     // B rows past the last token: zero codes; their scales: zero
     for (int c = tid; c < nkb * (N - mvalid) * 8; c += kStreamThreads) {
         const int kbl = c / ((N - mvalid) * 8), r2 = c - kbl * ((N - mvalid) * 8);
