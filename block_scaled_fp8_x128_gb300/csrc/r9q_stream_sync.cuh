@@ -20,12 +20,13 @@
 //    stages as its first act, before any block or cluster barrier; the cluster
 //    barrier and the dependency wait (griddepcontrol.wait) come after.  The
 //    CTA's activation slice then arrives in shared memory with one bulk copy
-//    per token row and serves every tile of the CTA.  W8A8: each 128-wide group is quantised in place
-//    once per CTA at the A-load (shuffle amax, fp32-division-exact quotient,
+//    per token row and serves every tile of the CTA.  W8A8: each 128-wide
+//    group is quantised in place once per CTA at the A-load, spread over all
+//    warps (shuffle amax, fp32-division-exact quotient,
 //    cvt.rn.satfinite.e4m3x2), byte-identical to the standalone quant kernel.
 //    Weight-only: the bf16 rows are the B operand, their pairs swapped in
 //    registers to match the in-register e4m3 -> bf16 conversion.
-//  * eight MMA warps (16 weight rows each; the row-group count kRowGroups
+//  * eight MMA warps (16 weight rows each; the row-group count kSyncRowGroups
 //    lets a warp hold several 16-row groups that share its activation
 //    fragments, measured slower) run swap-AB mma.sync (weights are the 16-row
 //    A operand, tokens the 8-column B operand): m16n8k32 e4m3 for W8A8,
