@@ -82,39 +82,10 @@ struct Params {
     int* err;
 };
 
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-    // K-major operand, 128-byte swizzle: 8-row x 128-byte atoms stacked every
-    // 1024 bytes (stride byte offset); the leading byte offset is unused.
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(16u >> 4) << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;                     // SWIZZLE_128B
-    return d;
-}
-
-// kind::f8f6f4 instruction descriptor: D fp32, A and B e4m3, both K-major,
-// N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// kind::f8f6f4 instruction descriptor of the 128 x 256 tile (D fp32, A and B
+// e4m3, both K-major); the shared-memory descriptors, the MMA issue, the
+// commits and the tcgen05 fences are r9q_device.cuh's umma_* helpers.
+constexpr uint32_t kIdesc = umma_idesc_e4m3(BM, BN);
 
 // 32 consecutive TMEM columns of this thread's lane.  The load is asynchronous:
 // its registers may be used only after a tmem_wait that names them.
@@ -293,15 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         flags[0] = flags[1] = flags[2] = 0;
         fence_proxy_async_smem();
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    umma_fence_before();
     __syncthreads();
-    tc_fence_after();
+    umma_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (fused) {
@@ -428,15 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             fail();
                             break;
                         }
-                        tc_fence_after();
+                        umma_fence_after();
                         const uint32_t sa = smem_u32(ring + st * kTcStageBytes);
                         const uint32_t sb = sa + kABytes;
                         const uint32_t td = tmem_base + (uint32_t)(ab * BN);
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k)
-                            mma_f8(td, sdesc_sw128(sa + k * 32), sdesc_sw128(sb + k * 32), k > 0 ? 1u : 0u);
-                        mma_commit(&empty[st]);      // stage free once these MMAs have read it
-                        mma_commit(&tfull[ab]);      // partial ready for the epilogue
+                            umma_e4m3(td, umma_sdesc_sw128(sa + k * 32), umma_sdesc_sw128(sb + k * 32), kIdesc,
+                                      k > 0 ? 1u : 0u);
+                        umma_commit(&empty[st]);      // stage free once these MMAs have read it
+                        umma_commit(&tfull[ab]);      // partial ready for the epilogue
                         flags[2] = it + 1;
                     }
                     if (*vflags) break;
@@ -497,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ab = it & 1;
                 const float sc = as_col[kb * (BM + 1)] * ws_wg[kb];
                 if (*vflags == 0 && !mbar_wait_sleep(&tfull[ab], (uint32_t)(it >> 1) & 1u)) fail();
-                tc_fence_after();
+                umma_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * BN + wg * 128);
                 // Two 32-column loads in flight at a time: the FMAs of one
                 // pair overlap the TMEM latency of the next.
@@ -512,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait(ra, rb);
                 // the whole partial is in registers: free the buffer for the
                 // MMA two k-blocks ahead before the last FMAs
-                tc_fence_before();
+                umma_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[ab]);
                 promote32(acc + 64, ra, sc);
@@ -605,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- teardown ----------------
-    tc_fence_before();
+    umma_fence_before();
     __syncthreads();
     if (flags[0] != 0 && tid == 0) {
         // drain what was issued: ring copies, then the MMAs' last commits
@@ -632,10 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    tc_fence_after();
-    if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
-                     : "memory");
+    umma_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
 size_t tc_smem_bytes() { return 1024 + (size_t)kStages * kTcStageBytes + kOutBytes + kAsBytes + kWsBytes + 256; }
